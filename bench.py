@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Throughput of the Muon step over stacked parameter banks on GB300.
+
+One step ("bank-step") = one muon_multi_step over every bank of the
+GPT-2-small Muon parameter set: the attention bank (40, 768, 768), the MLP
+bank (24, 3072, 768) with its dead slot, smear_gate (1, 12, 768) and
+attn_gate (10, 6, 12): momentum, Frobenius normalisation, five quintic
+Newton-Schulz iterations and the bf16 + mantissa update, all in this
+repository's CUDA kernels.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--workload 4|5]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (the step has no cross-GPU exchange on one node's banks);
+the value is all ranks' steps divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon bank-steps/sec & NS TFLOP/s vs bf16 peak; update GB/s vs HBM peak"
+UNIT = "bank-steps/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NS_GEMM_SOURCES = ["newton_schulz_stacked_gb300/csrc/mb_ns_gemm.cu", "newton_schulz_stacked_gb300/csrc/mb_device.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", type=int, default=4, choices=[4, 5])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- work counts
+
+def shapes_of(wl):
+    return [(b.batch, b.rows, b.cols) for b in wl.banks]
+
+
+def ns_flops(shapes, ns_steps):
+    """Algorithmic Newton-Schulz flops per step (3 m^2 n + m^3 per matrix and iteration: A and A^2
+    counted once, symmetric) split by phase, and the dense-equivalent total (4 m^2 n + 2 m^3)."""
+    gram = poly = apply_ = small = dense = 0.0
+    for (B, R, C) in shapes:
+        m, n = min(R, C), max(R, C)
+        if m <= 64:
+            small += B * ns_steps * (3.0 * m * m * n + m ** 3)
+            continue
+        gram += B * ns_steps * m * m * n
+        poly += B * ns_steps * float(m) ** 3
+        apply_ += B * ns_steps * 2.0 * m * m * n
+        dense += B * ns_steps * (4.0 * m * m * n + 2.0 * m ** 3)
+    return dict(gram=gram, poly=poly, apply=apply_, small=small, gemm=gram + poly + apply_, dense_gemm=dense)
+
+
+def elems(shapes):
+    return sum(B * R * C for (B, R, C) in shapes)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in NS_GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per NS GEMM launch from the committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_sha") != kernel_hash():
+        return None
+    return d.get("workloads", {}).get(str(workload), {}).get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [ln.strip().split(", ") for ln in f if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+
+def cpu_oracle_sample(wl, per_bank, seed_step=1):
+    """Time the fp64 oracle on a bounded sample of the workload; extrapolate to one full step."""
+    import numpy as np
+    import oracle as O
+    import synth
+    total_est, sampled, desc = 0.0, 0, []
+    for bi, spec in enumerate(wl.banks):
+        n = min(per_bank.get(spec.name, 1), spec.batch)
+        rng = np.random.default_rng(seed_step * 100 + bi)
+        idx = sorted(rng.choice(spec.batch, size=n, replace=False).tolist())
+        one = synth.BankSpec(spec.name, 1, spec.rows, spec.cols, spec.grad_kind, spec.grad_std)
+        w, mant, mom, row = synth.draw_state(rng, one)
+        g = synth.draw_grad(rng, one)
+        t0 = time.perf_counter()
+        for _ in idx:
+            O.bank_step(w, mant, mom, g, wl.lr, wl.wd, wl.mu, wl.ns_steps,
+                        normuon_beta2=wl.beta2 if wl.normuon else None, row_state=row)
+        dt = time.perf_counter() - t0
+        total_est += dt / n * spec.batch
+        sampled += n
+        desc.append(f"{n}/{spec.batch} of {spec.name}")
+    return total_est, sampled, ", ".join(desc)
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    sample = {"attn": 1, "mlp": 1, "smear_gate": 1, "attn_gate": 10}
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, sample, seed_step=0)
+    ests = []
+    desc = ""
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        est, _, desc = cpu_oracle_sample(wl, sample, seed_step=k + 1)
+        ests.append(est)
+    wall = time.perf_counter() - t0
+    est = statistics.mean(ests)
+    value = 1.0 / est
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64 banks)",
+        "config": config_of(wl, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                         "sample": f"each step times the fp64 oracle on {desc} and scales to the full step; "
+                                   f"{args.steps} steps took {wall:.1f} s"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, args):
+    return {
+        "workload": f"{wl.name}: " + " + ".join(f"{b.name} {b.batch}x{b.rows}x{b.cols}" for b in wl.banks),
+        "banks": [{"name": b.name, "shape": [b.batch, b.rows, b.cols], "grad": b.grad_kind,
+                   "dead_slots": list(b.dead_slots)} for b in wl.banks],
+        "ns_steps": wl.ns_steps, "lr": wl.lr, "wd": wl.wd, "mu": wl.mu, "normuon": wl.normuon,
+        "l2": "no flush: inputs larger than L2 (%.2f GB of step state read and written per step)" % (
+            elems(shapes_of(wl)) * (2 + 2 + 4 + 2) / 1e9),
+        "parallelism": f"replicas x{args.gpus}",
+    }
+
+
+# ---------------------------------------------------------------- native arm
+
+def run_native(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import newton_schulz_stacked_gb300 as nss
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    nss.load_library()
+
+    wl = synth.WORKLOADS[args.workload]
+    shapes = shapes_of(wl)
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    banks, grads, grads_host = [], [], []
+    for bi, spec in enumerate(wl.banks):
+        w, mant, mom, row = synth.init_state(wl.wid, bi)
+        g_steps = [synth.grad(wl.wid, s, bi) for s in (1, 2)]
+        grads.append([t16(g) for g in g_steps])
+        grads_host.append([torch.from_numpy(g.view(np.int16)).pin_memory() for g in g_steps])
+        banks.append(nss.BankState(t16(w), grads[-1][0], torch.from_numpy(mom).to(dev), t16(mant),
+                                   torch.from_numpy(row).to(dev) if wl.normuon else None))
+    ws = torch.empty(nss.mb_multi_workspace_bytes(banks, wl.normuon), dtype=torch.uint8, device=dev)
+
+    def step(k):
+        for b, g in zip(banks, grads):
+            b.grad = g[k & 1]
+        nss.muon_multi_step(banks, wl.lr, wl.wd, wl.mu, normuon=wl.normuon, beta2=wl.beta2, ns_steps=wl.ns_steps,
+                            workspace=ws)
+
+    for k in range(max(args.warmup, 3)):
+        step(k)
+    torch.cuda.synchronize()
+    if nss.mb_sync_status() != 0:
+        raise RuntimeError("device-side status set during warm-up")
+
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = nss.mb_launch_count()
+    with ClockSampler(torch.cuda.current_device() if world == 1 else local) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with nss.StageTimer(max_marks=64 * args.steps + 64) as timer:
+            ev0.record(stream)
+            for k in range(args.steps):
+                step(k)
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    launches = nss.mb_launch_count() - n0
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    if nss.mb_sync_status() != 0:
+        raise RuntimeError("device-side status set during the timed steps")
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * args.steps / (elapsed_ms / 1e3)
+
+    # per-stage device time from the library's stage events (same stream, same timed steps)
+    tot = timer.totals()
+    per = {k: v[0] / args.steps for k, v in tot.items()}
+    gemm_ms = per.get("gram", 0.0) + per.get("poly", 0.0) + per.get("apply", 0.0)
+    gemm_launches = sum(tot.get(k, (0, 0))[1] for k in ("gram", "poly", "apply"))
+    fl = ns_flops(shapes, wl.ns_steps)
+    E = elems(shapes)
+    pk, pk_kind = peaks()
+    tensor_peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    hbm_peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    ns_tflops = fl["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
+    mom_gbs = 12.0 * E / (per["momentum"] * 1e-3) / 1e9 if per.get("momentum") else None
+    upd_gbs = 10.0 * E / (per["update"] * 1e-3) / 1e9 if per.get("update") else None
+    per_launch_flops = fl["gemm"] * args.steps / max(gemm_launches, 1)
+    per_launch_ms = gemm_ms * args.steps / max(gemm_launches, 1)
+
+    roofline = {
+        "bound": "tensor", "kernel": "ns_gemm_kernel (A=XX^T, B=bA+cAA, X=aX+BX; %d launches per step)" % (
+            gemm_launches // args.steps),
+        "achieved": ns_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
+        "frac": (ns_tflops / tensor_peak) if ns_tflops else None,
+        "peak_kind": f"{pk_kind} bf16 sustained (kernel timed inside a long step loop)",
+        "flops_per_launch": per_launch_flops, "ms_per_launch": per_launch_ms,
+        "traffic": profiled_traffic(args.workload),
+    }
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = {"attn": 8, "mlp": 4, "smear_gate": 1, "attn_gate": 10} if args.workload == 4 else \
+            {"attn": 4, "mlp": 2}
+        t0 = time.perf_counter()
+        est, _, desc = cpu_oracle_sample(wl, sample)
+        cpu_base = {"value": 1.0 / est, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                    "sample": f"fp64 oracle on {desc} ({time.perf_counter() - t0:.1f} s), scaled to one full step"}
+
+    e2e = None
+    if not args.no_e2e:
+        bank_host = [torch.empty(b.bank.shape, dtype=torch.int16).pin_memory() for b in banks]
+        h2d = sum(g[0].numel() * 2 for g in grads_host)
+        d2h = sum(b.numel() * 2 for b in bank_host)
+        k_e2e = max(1, min(args.steps, 50))
+        for k in range(3):
+            for b, gh in zip(banks, grads_host):
+                b.grad.copy_(gh[k & 1], non_blocking=True)
+            step(k)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for k in range(k_e2e):
+            for b, g, gh in zip(banks, grads, grads_host):
+                g[k & 1].copy_(gh[k & 1], non_blocking=True)
+            step(k)
+            for b, bh in zip(banks, bank_host):
+                bh.copy_(b.bank, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * k_e2e / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": k_e2e,
+               "what": "pinned host gradients -> device, muon_multi_step, updated bf16 weights -> pinned host"}
+
+    if rank == 0:
+        line = {
+            "impl": "native", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded PCG64 banks; low-rank-plus-noise gradients, two alternating steps)",
+            "config": config_of(wl, args),
+            "roofline": roofline,
+            "ns_tflops": ns_tflops,
+            "ns_tflops_dense_equiv": fl["dense_gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None,
+            "momentum_gbs": mom_gbs, "update_gbs": upd_gbs,
+            "fractions": {"ns_of_bf16_sustained": (ns_tflops / tensor_peak) if ns_tflops else None,
+                          "momentum_of_hbm": (mom_gbs / hbm_peak) if mom_gbs else None,
+                          "update_of_hbm": (upd_gbs / hbm_peak) if upd_gbs else None, "peaks": pk_kind},
+            "stages_ms_per_step": per,
+            "cpu_baseline": cpu_base,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * muonbank.h -- C ABI of libmuonbank.so: the Muon optimizer step over stacked
+ * parameter banks on one NVIDIA GB300 (sm_103a).
+ *
+ * What one step computes, for every matrix X of a bank [batch, rows, cols]
+ * independently (sources by page and section):
+ *   S1  momentum   buf <- lerp(buf, g, 1-mu);  u <- lerp(g, buf, mu)
+ *                  ("Muon Custom Sizing" write-up, record 2025-09-23, section 4,
+ *                  second pass; Nesterov form named in the "UNetDoubleLr"
+ *                  write-up, record 2024-11-10, optimizer section)
+ *   S2  normalise  X0 = u / (||u||_F + 1e-7)  (the pages normalise by the
+ *                  spectral norm; the Frobenius norm bounds it from above)
+ *   S3  orientation: a tall matrix (rows > cols) iterates on X^T, which the
+ *                  kernels realise as the swapped-operand form, with no copy
+ *   S4  quintic Newton-Schulz, ns_steps times (5 by default):
+ *                  A = X X^T;  B = b A + c A A;  X <- a X + B X,
+ *                  (a, b, c) = (3.4445, -4.7750, 2.0315)
+ *                  ("Muon Custom Sizing" write-up, section 2.3; Track-2
+ *                  record 7 write-up, 2025-04-16, section 4.2)
+ *                  Operands and stored A, B, X are bf16, with fp32
+ *                  accumulation and fp32 epilogue arithmetic; matrices with
+ *                  min(rows, cols) <= 64 run the whole iteration in fp32.
+ *   S5  update     w32 = (w_bf16_bits << 16) | mantissa;
+ *                  w32 <- w32 * (1 - lr*wd);  w32 <- w32 - lr*sqrt(max(1, rows/cols)) * v;
+ *                  w_bf16_bits = w32 >> 16;  mantissa = w32 & 0xFFFF
+ *                  (Track-2 record 7 write-up, section 4.1; effective lr and
+ *                  decay from the "Muon Custom Sizing" write-up, section 4)
+ *   S6  NorMuon (normuon_bank_step only; the "Unified zero-copy optimizer"
+ *                  write-up, record 2026-01-18, names NorMuon but gives no
+ *                  formula; this library reads it as): per row i of the
+ *                  stored matrix q_i = mean_j v_ij^2, s_i <- beta2 s_i +
+ *                  (1-beta2) q_i, v_ij <- v_ij / sqrt(max(s_i, 1e-10)), then
+ *                  v is rescaled to its Frobenius norm before S6.
+ *
+ * Conventions shared by every entry point
+ *   - Buffers are device pointers owned by the caller, row-major and
+ *     contiguous: matrix k of a bank starts at k*rows*cols elements.  bf16
+ *     tensors are passed as raw 16-bit patterns.  Every pointer must be
+ *     16-byte aligned.
+ *   - The library never allocates.  Scratch is a caller-provided device
+ *     workspace of at least the size the *_workspace_bytes query returns;
+ *     its contents need no initialisation and are overwritten.
+ *   - Calls enqueue work on `cuda_stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and return without synchronising the host.
+ *   - Return value: MB_OK (0) or a negative MB_ERR_* code.  Argument errors
+ *     are detected before anything is enqueued.  A launch failure returns
+ *     MB_ERR_CUDA (text from mb_last_cuda_error()).  A device-side fault
+ *     detected while running (a bounded wait that expired) is latched in a
+ *     per-device error word and returned by mb_sync_status().
+ *   - Results are bit-identical from run to run (no float atomics).
+ *   - In-place state (bank, mantissa, momentum, row state) must not alias
+ *     any other argument.
+ */
+#ifndef MUONBANK_H_
+#define MUONBANK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MB_OK = 0,
+  MB_ERR_NULL = -1,          /* a required pointer is NULL */
+  MB_ERR_SHAPE = -2,         /* batch/rows/cols <= 0, or an element count that overflows */
+  MB_ERR_ALIGN = -3,         /* a pointer is not 16-byte aligned */
+  MB_ERR_NS_STEPS = -4,      /* ns_steps outside 0..16 */
+  MB_ERR_WORKSPACE = -5,     /* workspace NULL or smaller than required */
+  MB_ERR_CUDA = -6,          /* a CUDA runtime call or kernel launch failed */
+  MB_ERR_TIMEOUT = -7,       /* a device-side bounded wait expired (from mb_sync_status) */
+  MB_ERR_ARG = -8,           /* a scalar argument is not finite, or beta2/mu outside [0, 1] */
+  MB_ERR_UNSUPPORTED = -9,   /* the current device is not sm_103 */
+  MB_ERR_TOO_MANY = -10      /* more banks than one call accepts */
+};
+
+/* One bank: `batch` matrices of rows x cols. */
+typedef struct {
+  int32_t batch, rows, cols;
+} mb_shape;
+
+/* One bank of a multi-bank call (the launch sequence of a whole model step). */
+typedef struct {
+  void* bank;            /* bf16 [batch, rows, cols], updated in place */
+  const void* grad;      /* bf16 [batch, rows, cols], read only */
+  float* momentum;       /* fp32 [batch, rows, cols], updated in place */
+  uint16_t* mantissa;    /* uint16 [batch, rows, cols], updated in place */
+  float* row_state;      /* fp32 [batch, rows] NorMuon second moment; NULL unless normuon */
+  mb_shape shape;
+} mb_bank_desc;
+
+#define MB_MAX_BANKS 8
+
+/* Bytes of workspace that muon_bank_step (normuon = 0) or normuon_bank_step
+ * (normuon = 1) needs for `shape`. */
+int mb_workspace_bytes(mb_shape shape, int normuon, size_t* out_bytes);
+
+/* One full Muon step (S1-S5) over a bank.  lr and wd are the caller's values
+ * with any per-parameter multipliers folded in; mu is the momentum of this
+ * step (the caller applies any warm-up).  ns_steps = 0 skips S4 (v = X0). */
+int muon_bank_step(void* bank_bf16, const void* grad_bf16, float* momentum_f32,
+                   uint16_t* mantissa, mb_shape shape, float lr, float wd, float mu,
+                   int ns_steps, void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Muon step with the NorMuon per-row normalisation (S1-S4, S6, S5).
+ * row_state_f32 is [batch, rows], updated in place; beta2 in [0, 1]. */
+int normuon_bank_step(void* bank_bf16, const void* grad_bf16, float* momentum_f32,
+                      uint16_t* mantissa, float* row_state_f32, mb_shape shape, float lr,
+                      float wd, float mu, float beta2, int ns_steps, void* workspace,
+                      size_t workspace_bytes, void* cuda_stream);
+
+/* Workspace for muon_multi_step over `n_banks` descriptors. */
+int mb_multi_workspace_bytes(const mb_bank_desc* banks, int n_banks, int normuon,
+                             size_t* out_bytes);
+
+/* One step over up to MB_MAX_BANKS banks with shared hyperparameters, as one
+ * launch sequence: the element-wise stages run once over all banks and the
+ * Newton-Schulz GEMMs of all large banks share each launch.  normuon selects
+ * S6 for every bank (each then needs row_state).  The `banks` array is read on
+ * the host during the call only. */
+int muon_multi_step(const mb_bank_desc* banks, int n_banks, float lr, float wd, float mu,
+                    int normuon, float beta2, int ns_steps, void* workspace,
+                    size_t workspace_bytes, void* cuda_stream);
+
+/* ---- single stages, for callers that run them separately (and for tests) ---- */
+
+/* S1 only: momentum in place and u (bf16 [batch, rows, cols], dense) out. */
+int mb_momentum(const void* grad_bf16, float* momentum_f32, void* u_bf16, mb_shape shape,
+                float mu, void* cuda_stream);
+
+/* S2-S4 only: v = NS(u / (||u||_F + 1e-7)) per matrix, v bf16 dense [batch, rows, cols].
+ * Uses the muon_bank_step workspace (normuon = 0). */
+int mb_newton_schulz(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps,
+                     void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* S5 only, given v (bf16 dense). */
+int mb_update(void* bank_bf16, uint16_t* mantissa, const void* v_bf16, mb_shape shape,
+              float lr, float wd, void* cuda_stream);
+
+/* S6 then S5, given v (bf16 dense); uses the normuon_bank_step workspace. */
+int mb_normuon_update(void* bank_bf16, uint16_t* mantissa, const void* v_bf16,
+                      float* row_state_f32, mb_shape shape, float lr, float wd, float beta2,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Where a finished muon_bank_step / normuon_bank_step left u (the bf16 NS
+ * input) and v (the bf16 NS output) inside its workspace: byte offsets from
+ * the workspace start and the row pitch in elements (>= cols); matrix k of
+ * each starts at k * rows * pitch elements. */
+int mb_workspace_views(mb_shape shape, int normuon, int ns_steps, size_t* u_offset,
+                       size_t* v_offset, size_t* row_pitch);
+
+/* Synchronises `cuda_stream`, then returns and clears this device's latched
+ * device-side status (MB_OK or MB_ERR_TIMEOUT), or MB_ERR_CUDA. */
+int mb_sync_status(void* cuda_stream);
+
+/* Runs the bounded-wait primitive of the kernels against an mbarrier that
+ * nothing completes, with a limit of `limit_us` microseconds; the kernel gives
+ * up, latches MB_ERR_TIMEOUT and returns.  For testing failure detection. */
+int mb_selftest_timeout(unsigned limit_us, void* cuda_stream);
+
+/* ---- measurement hooks ---- */
+
+/* Number of kernels this host thread has launched through the library so far. */
+uint64_t mb_launch_count(void);
+
+/* Stage labels of the timing marks. */
+enum {
+  MB_MARK_BEGIN = 0,      /* start of a step (or stage call) */
+  MB_MARK_MOMENTUM = 1,   /* after S1 (and the u^2 partial sums) */
+  MB_MARK_SCALE = 2,      /* after the per-matrix 1/(||u||+eps) */
+  MB_MARK_SMALL_NS = 3,   /* after the fp32 Newton-Schulz of small matrices */
+  MB_MARK_GRAM = 4,       /* after one A = X X^T launch */
+  MB_MARK_POLY = 5,       /* after one B = bA + cAA launch */
+  MB_MARK_APPLY = 6,      /* after one X <- aX + BX launch */
+  MB_MARK_NS0 = 7,        /* after the ns_steps = 0 scaling */
+  MB_MARK_ROWSTATS = 8,   /* after the NorMuon row statistics */
+  MB_MARK_UPDATE = 9      /* after S5 */
+};
+
+/* Starts recording a CUDA event on the launching stream at every stage
+ * boundary of the following calls made by this host thread, up to
+ * `max_marks` marks (events are created here; no device memory is allocated). */
+int mb_timing_begin(int max_marks);
+
+/* Stops recording, synchronises the events and returns up to `cap` marks:
+ * labels[i] (MB_MARK_*) and ms[i] = milliseconds from the previous mark to
+ * mark i (0 for MB_MARK_BEGIN).  *n_marks receives the number recorded. */
+int mb_timing_end(int cap, int* labels, float* ms, int* n_marks);
+
+/* Static text of a status code; the last CUDA error message of this thread. */
+const char* mb_status_string(int status);
+const char* mb_last_cuda_error(void);
+
+/* Library version, (major << 16) | minor. */
+int mb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUONBANK_H_ */

@@ -1,0 +1,229 @@
+"""GB300-native Muon step over stacked parameter banks.
+
+Thin Python face of libmuonbank.so: each function has the name of the C
+entry point it calls, takes CUDA tensors (bf16 banks may be passed as
+torch.bfloat16, int16 or uint16 tensors: only the bits matter) and enqueues
+the work on the current CUDA stream.  All arithmetic runs in the library's
+kernels.  Buffers are the caller's; a workspace tensor is created with
+torch only when the caller does not pass one.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _binding as _b
+from ._binding import MuonBankError, MB_MAX_BANKS  # noqa: F401
+
+__all__ = [
+    "muon_bank_step", "normuon_bank_step", "muon_multi_step", "mb_workspace_bytes",
+    "mb_multi_workspace_bytes", "mb_momentum", "mb_newton_schulz", "mb_update", "mb_normuon_update",
+    "mb_workspace_views", "mb_sync_status", "mb_selftest_timeout", "mb_status_string", "MuonBankError",
+    "BankState", "load_library", "mb_launch_count", "StageTimer",
+]
+
+_TWO_BYTE = (torch.bfloat16, torch.int16, torch.uint16, torch.float16)
+
+
+def load_library():
+    return _b.load()
+
+
+def _ptr(t: Optional[torch.Tensor], dtypes, what: str) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{what} has dtype {t.dtype}, expected one of {dtypes}")
+    return t.data_ptr()
+
+
+def _shape(t: torch.Tensor) -> _b.MbShape:
+    if t.dim() == 2:
+        return _b.shape_of(1, t.shape[0], t.shape[1])
+    if t.dim() != 3:
+        raise ValueError("a bank is [batch, rows, cols] (or one [rows, cols] matrix)")
+    return _b.shape_of(*t.shape)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _workspace(nbytes: int, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
+    if workspace is None:
+        return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, needs {nbytes}")
+    return workspace
+
+
+def mb_status_string(status: int) -> str:
+    return _b.load().mb_status_string(status).decode()
+
+
+def mb_workspace_bytes(shape, normuon: bool = False) -> int:
+    out = ctypes.c_size_t(0)
+    _b.check("mb_workspace_bytes", _b.load().mb_workspace_bytes(_b.shape_of(*shape), int(normuon), ctypes.byref(out)))
+    return out.value
+
+
+def muon_bank_step(bank, grad, momentum, mantissa, lr: float, wd: float, mu: float, ns_steps: int = 5,
+                   workspace=None, stream=None):
+    """One Muon step over the bank, in place (bank, momentum, mantissa)."""
+    sh = _shape(bank)
+    ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols)), workspace, bank.device)
+    st = _b.load().muon_bank_step(
+        _ptr(bank, _TWO_BYTE, "bank"), _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"),
+        _ptr(mantissa, _TWO_BYTE, "mantissa"), sh, lr, wd, mu, ns_steps, ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream))
+    _b.check("muon_bank_step", st)
+    return ws
+
+
+def normuon_bank_step(bank, grad, momentum, mantissa, row_state, lr: float, wd: float, mu: float,
+                      beta2: float = 0.95, ns_steps: int = 5, workspace=None, stream=None):
+    """One Muon step with NorMuon per-row normalisation, in place (row_state too)."""
+    sh = _shape(bank)
+    ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols), True), workspace, bank.device)
+    st = _b.load().normuon_bank_step(
+        _ptr(bank, _TWO_BYTE, "bank"), _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"),
+        _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(row_state, (torch.float32,), "row_state"), sh, lr, wd, mu,
+        beta2, ns_steps, ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+    _b.check("normuon_bank_step", st)
+    return ws
+
+
+class BankState:
+    """The caller-owned tensors of one bank: bank, grad, momentum, mantissa (and row_state)."""
+
+    def __init__(self, bank, grad, momentum, mantissa, row_state=None):
+        self.bank, self.grad, self.momentum, self.mantissa, self.row_state = bank, grad, momentum, mantissa, row_state
+
+    def desc(self) -> _b.MbBankDesc:
+        return _b.MbBankDesc(_ptr(self.bank, _TWO_BYTE, "bank"), _ptr(self.grad, _TWO_BYTE, "grad"),
+                             _ptr(self.momentum, (torch.float32,), "momentum"),
+                             _ptr(self.mantissa, _TWO_BYTE, "mantissa"),
+                             _ptr(self.row_state, (torch.float32,), "row_state"), _shape(self.bank))
+
+
+def _descs(banks: Sequence[BankState]):
+    arr = (_b.MbBankDesc * len(banks))()
+    for i, b in enumerate(banks):
+        arr[i] = b.desc()
+    return arr
+
+
+def mb_multi_workspace_bytes(banks: Sequence[BankState], normuon: bool = False) -> int:
+    out = ctypes.c_size_t(0)
+    _b.check("mb_multi_workspace_bytes",
+             _b.load().mb_multi_workspace_bytes(_descs(banks), len(banks), int(normuon), ctypes.byref(out)))
+    return out.value
+
+
+def muon_multi_step(banks: Sequence[BankState], lr: float, wd: float, mu: float, normuon: bool = False,
+                    beta2: float = 0.95, ns_steps: int = 5, workspace=None, stream=None):
+    """One step over several banks as one launch sequence."""
+    arr = _descs(banks)
+    ws = _workspace(mb_multi_workspace_bytes(banks, normuon), workspace, banks[0].bank.device)
+    st = _b.load().muon_multi_step(arr, len(banks), lr, wd, mu, int(normuon), beta2, ns_steps, ws.data_ptr(),
+                                   ws.numel() * ws.element_size(), _stream(stream))
+    _b.check("muon_multi_step", st)
+    return ws
+
+
+def mb_momentum(grad, momentum, u, mu: float, stream=None):
+    sh = _shape(grad)
+    _b.check("mb_momentum", _b.load().mb_momentum(
+        _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"), _ptr(u, _TWO_BYTE, "u"), sh,
+        mu, _stream(stream)))
+
+
+def mb_newton_schulz(u, v, ns_steps: int = 5, workspace=None, stream=None):
+    sh = _shape(u)
+    ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols)), workspace, u.device)
+    _b.check("mb_newton_schulz", _b.load().mb_newton_schulz(
+        _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, ns_steps, ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return ws
+
+
+def mb_update(bank, mantissa, v, lr: float, wd: float, stream=None):
+    sh = _shape(bank)
+    _b.check("mb_update", _b.load().mb_update(
+        _ptr(bank, _TWO_BYTE, "bank"), _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(v, _TWO_BYTE, "v"), sh, lr, wd,
+        _stream(stream)))
+
+
+def mb_normuon_update(bank, mantissa, v, row_state, lr: float, wd: float, beta2: float = 0.95, workspace=None,
+                      stream=None):
+    sh = _shape(bank)
+    ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols), True), workspace, bank.device)
+    _b.check("mb_normuon_update", _b.load().mb_normuon_update(
+        _ptr(bank, _TWO_BYTE, "bank"), _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(v, _TWO_BYTE, "v"),
+        _ptr(row_state, (torch.float32,), "row_state"), sh, lr, wd, beta2, ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return ws
+
+
+def mb_workspace_views(shape, normuon: bool = False, ns_steps: int = 5):
+    """(u byte offset, v byte offset, row pitch in elements) inside a step's workspace."""
+    u, v, p = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _b.check("mb_workspace_views", _b.load().mb_workspace_views(
+        _b.shape_of(*shape), int(normuon), ns_steps, ctypes.byref(u), ctypes.byref(v), ctypes.byref(p)))
+    return u.value, v.value, p.value
+
+
+def mb_sync_status(stream=None) -> int:
+    return _b.load().mb_sync_status(_stream(stream))
+
+
+def mb_selftest_timeout(limit_us: int, stream=None):
+    _b.check("mb_selftest_timeout", _b.load().mb_selftest_timeout(limit_us, _stream(stream)))
+
+
+def mb_launch_count() -> int:
+    """Kernels this thread has launched through the library so far."""
+    return int(_b.load().mb_launch_count())
+
+
+class StageTimer:
+    """Records CUDA events at the library's stage boundaries while active.
+
+    with StageTimer(max_marks) as t: ...steps...
+    t.marks -> list of (stage name, ms since the previous mark)
+    """
+
+    def __init__(self, max_marks: int = 4096):
+        self.max_marks = max_marks
+        self.marks = []
+
+    def __enter__(self):
+        _b.check("mb_timing_begin", _b.load().mb_timing_begin(self.max_marks))
+        return self
+
+    def __exit__(self, *exc):
+        n = self.max_marks
+        labels = (ctypes.c_int * n)()
+        ms = (ctypes.c_float * n)()
+        got = ctypes.c_int(0)
+        _b.check("mb_timing_end", _b.load().mb_timing_end(n, labels, ms, ctypes.byref(got)))
+        self.marks = [(_b.MARK_NAMES.get(labels[i], str(labels[i])), float(ms[i])) for i in range(min(got.value, n))]
+        return False
+
+    def totals(self):
+        """Per stage: (total ms, number of marks)."""
+        out = {}
+        for name, ms in self.marks:
+            if name == "begin":
+                continue
+            t, c = out.get(name, (0.0, 0))
+            out[name] = (t + ms, c + 1)
+        return out

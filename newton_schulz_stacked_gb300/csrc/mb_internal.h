@@ -1,0 +1,131 @@
+// Internal interfaces between the C ABI (mb_api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mb {
+
+constexpr int MAX_BANKS = 8;       // banks per element-wise launch
+constexpr int MAX_GEMM_PROBS = 4;  // banks per Newton-Schulz GEMM launch
+constexpr int SMALL_M = 64;        // min(rows, cols) <= SMALL_M: fp32 SIMT Newton-Schulz
+
+// Elements handled by one block of the element-wise kernels (per matrix chunk).
+constexpr int EW_THREADS = 256;
+constexpr int EW_CHUNK = EW_THREADS * 8 * 4;
+
+// ---------------------------------------------------------------- element-wise stages
+
+struct EwBank {
+  const uint16_t* src;     // K1: grad (momentum) or u (pack); K3: unused
+  float* mom;              // K1 momentum (null in pack mode)
+  uint16_t* bank;          // K3 weight bf16 bits
+  uint16_t* mant;          // K3 mantissa
+  uint16_t* xout;          // K1: u destination (pitch ld); ns0/unpack: destination
+  const uint16_t* xin;     // K3/ns0/unpack: source (pitch ld)
+  const float* rowscale;   // K3 NorMuon per-row factor (null otherwise)
+  float* partials;         // K1: per-chunk sum of u^2, [batch * P] (null = skip)
+  const float* scale;      // ns0: per-matrix 1/(||u||+eps)
+  int batch, rows, cols, ld, out_ld;
+  int P;                   // chunks per matrix
+  int block_begin;         // first block of this bank in the launch
+  float decay, neg_lr;     // K3: 1 - lr*wd, -lr*sqrt(max(1, rows/cols))
+};
+
+struct EwParams {
+  EwBank b[MAX_BANKS];
+  int nb;
+  int total_blocks;
+  float mu, omm;           // K1: momentum and 1 - mu (formed in double on the host)
+  int* status;
+};
+
+// Per-matrix scale s = 1/(sqrt(sum partials) + eps).
+struct ScaleBank {
+  const float* partials;
+  float* scale;
+  int batch, P, mat_begin;
+};
+struct ScaleParams {
+  ScaleBank b[MAX_BANKS];
+  int nb, total_mats;
+};
+
+// fp32 SIMT Newton-Schulz for small matrices: one block per matrix.
+struct SmallBank {
+  const uint16_t* x0;   // u, bf16, pitch ld
+  float* xf0;           // fp32 scratch [batch, rows, cols]
+  float* xf1;
+  uint16_t* out;        // bf16 result, pitch ld
+  const float* scale;
+  int batch, rows, cols, ld;
+  int block_begin;
+};
+struct SmallParams {
+  SmallBank b[MAX_BANKS];
+  int nb, total_blocks, steps;
+  float ca, cb, cc;
+};
+
+// NorMuon row statistics and scales.
+struct RowBank {
+  const uint16_t* v;    // NS output, pitch ld
+  float* q;             // per-row sum of v^2 [batch * rows]
+  float* state;         // row second moment [batch * rows] (in place)
+  float* rowscale;      // per-row factor [batch * rows]
+  int batch, rows, cols, ld;
+  int row_begin;        // prefix over rows (KN1) ...
+  int mat_begin;        // ... and over matrices (KN2)
+};
+struct RowParams {
+  RowBank b[MAX_BANKS];
+  int nb, total_rows, total_mats;
+  float beta2;
+};
+
+// ---------------------------------------------------------------- Newton-Schulz GEMMs
+
+enum GemmEpi { EPI_GRAM = 1, EPI_POLY = 2, EPI_APPLY = 3 };
+
+struct GemmProblem {
+  CUtensorMap map_a;     // operand A tiles
+  CUtensorMap map_b;     // operand B tiles
+  int a_mn, b_mn;        // 0: K-major tiles, 1: MN-major tiles
+  int M, N, K;
+  int batch;
+  int sym;               // upper-triangle 128-blocks, mirrored stores
+  int T;                 // sym: 128-blocks per side
+  int tn;                // dense: 256-wide column tiles
+  int tiles_per_mat;
+  int tile_begin;
+  uint16_t* out;         // bf16 output, pitch out_ld, matrix stride out_ms
+  long long out_ld, out_ms;
+  const uint16_t* ein;   // epilogue input (A for POLY, X for APPLY)
+  long long ein_ld, ein_ms;
+  const float* scale;    // per-matrix Frobenius scale (first iteration) or null
+};
+
+struct GemmParams {
+  GemmProblem prob[MAX_GEMM_PROBS];
+  int nprob;
+  int total_tiles;
+  float ca, cb, cc;
+  int* status;
+};
+
+// ---------------------------------------------------------------- launchers (return cudaError_t)
+
+cudaError_t launch_k1(const EwParams& p, bool momentum, cudaStream_t s);
+cudaError_t launch_scale(const ScaleParams& p, cudaStream_t s);
+cudaError_t launch_ns0(const EwParams& p, cudaStream_t s);
+cudaError_t launch_unpack(const EwParams& p, cudaStream_t s);
+cudaError_t launch_small_ns(const SmallParams& p, cudaStream_t s);
+cudaError_t launch_row_sumsq(const RowParams& p, cudaStream_t s);
+cudaError_t launch_row_scale(const RowParams& p, cudaStream_t s);
+cudaError_t launch_k3(const EwParams& p, bool normuon, cudaStream_t s);
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
+cudaError_t launch_gemm(const GemmParams& p, int epi, cudaStream_t s);
+
+}  // namespace mb
