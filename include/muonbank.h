@@ -72,7 +72,8 @@ enum {
   MB_ERR_TIMEOUT = -7,       /* a device-side bounded wait expired (from mb_sync_status) */
   MB_ERR_ARG = -8,           /* a scalar argument is not finite, or beta2/mu outside [0, 1] */
   MB_ERR_UNSUPPORTED = -9,   /* the current device is not sm_103 */
-  MB_ERR_TOO_MANY = -10      /* more banks than one call accepts */
+  MB_ERR_TOO_MANY = -10,     /* more banks than one call accepts */
+  MB_ERR_SCRATCH_LIMIT = -11 /* mb_newton_schulz_noalloc: the shape needs more than its fixed scratch */
 };
 
 /* One bank: `batch` matrices of rows x cols. */
@@ -133,6 +134,31 @@ int mb_momentum(const void* grad_bf16, float* momentum_f32, void* u_bf16, mb_sha
  * Uses the muon_bank_step workspace (normuon = 0). */
 int mb_newton_schulz(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps,
                      void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* S2-S4 like mb_newton_schulz, for callers that cannot allocate device memory.
+ *
+ * Not part of the method on the speedrun pages (they have no counterpart);
+ * it exists for callers that may not call cudaMalloc: code running inside a
+ * memory pool or allocator callback, a host whose allocator is owned by
+ * another framework, or a process that must not grow its device footprint
+ * after start-up.  Such callers cannot provide the workspace that
+ * mb_newton_schulz needs, so this variant uses a scratch array that the
+ * library holds as a fixed device global of MB_NOALLOC_SCRATCH_BYTES on every
+ * GPU that loads it, for the life of the process.  The caller still passes u
+ * and v (bf16 dense [batch, rows, cols]).
+ *   - Returns MB_ERR_SCRATCH_LIMIT, and enqueues nothing, when the shape needs
+ *     more scratch than that (mb_workspace_bytes(shape, 0) is the need).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, and it keeps the previous
+ *     call's contents.  Nothing in it has to start at zero (every byte is
+ *     written before it is read).  Calls that overlap on the GPU, from
+ *     different streams or threads, race on it: serialise them. */
+#define MB_NOALLOC_SCRATCH_BYTES (32u << 20)
+int mb_newton_schulz_noalloc(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps,
+                             void* cuda_stream);
 
 /* S5 only, given v (bf16 dense). */
 int mb_update(void* bank_bf16, uint16_t* mantissa, const void* v_bf16, mb_shape shape,

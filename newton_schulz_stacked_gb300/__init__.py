@@ -20,7 +20,7 @@ from ._binding import MuonBankError, MB_MAX_BANKS  # noqa: F401
 __all__ = [
     "muon_bank_step", "normuon_bank_step", "muon_multi_step", "mb_workspace_bytes",
     "mb_multi_workspace_bytes", "mb_momentum", "mb_newton_schulz", "mb_update", "mb_normuon_update",
-    "mb_workspace_views", "mb_sync_status", "mb_selftest_timeout", "mb_status_string", "MuonBankError",
+    "mb_newton_schulz_noalloc", "mb_workspace_views", "mb_sync_status", "mb_selftest_timeout", "mb_status_string", "MuonBankError",
     "BankState", "load_library", "mb_launch_count", "StageTimer",
 ]
 
@@ -153,6 +153,17 @@ def mb_newton_schulz(u, v, ns_steps: int = 5, workspace=None, stream=None):
         _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, ns_steps, ws.data_ptr(),
         ws.numel() * ws.element_size(), _stream(stream)))
     return ws
+
+
+def mb_newton_schulz_noalloc(u, v, ns_steps: int = 5, stream=None):
+    """mb_newton_schulz without a workspace, for callers that cannot allocate device memory.
+
+    The library serves the scratch from its fixed per-device array (at most
+    MB_NOALLOC_SCRATCH_BYTES); calls share it, so do not overlap them on the GPU.
+    """
+    sh = _shape(u)
+    _b.check("mb_newton_schulz_noalloc", _b.load().mb_newton_schulz_noalloc(
+        _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, ns_steps, _stream(stream)))
 
 
 def mb_update(bank, mantissa, v, lr: float, wd: float, stream=None):

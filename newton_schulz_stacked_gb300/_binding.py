@@ -26,6 +26,8 @@ MB_ERR_TIMEOUT = -7
 MB_ERR_ARG = -8
 MB_ERR_UNSUPPORTED = -9
 MB_ERR_TOO_MANY = -10
+MB_ERR_SCRATCH_LIMIT = -11
+MB_NOALLOC_SCRATCH_BYTES = 32 << 20
 MB_MAX_BANKS = 8
 
 
@@ -49,6 +51,7 @@ _SIGNATURES = {
                                 c_int, _P, c_size_t, _P]),
     "mb_momentum": (c_int, [_P, _P, _P, MbShape, c_float, _P]),
     "mb_newton_schulz": (c_int, [_P, _P, MbShape, c_int, _P, c_size_t, _P]),
+    "mb_newton_schulz_noalloc": (c_int, [_P, _P, MbShape, c_int, _P]),
     "mb_update": (c_int, [_P, _P, _P, MbShape, c_float, c_float, _P]),
     "mb_normuon_update": (c_int, [_P, _P, _P, _P, MbShape, c_float, c_float, c_float, _P, c_size_t, _P]),
     "mb_workspace_views": (c_int, [MbShape, c_int, c_int, ctypes.POINTER(c_size_t), ctypes.POINTER(c_size_t),

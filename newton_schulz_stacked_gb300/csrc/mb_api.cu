@@ -558,6 +558,7 @@ const char* mb_status_string(int status) {
     case MB_ERR_ARG: return "invalid scalar argument";
     case MB_ERR_UNSUPPORTED: return "device is not sm_103";
     case MB_ERR_TOO_MANY: return "too many banks in one call";
+    case MB_ERR_SCRATCH_LIMIT: return "shape needs more than the fixed no-alloc scratch (MB_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }
@@ -784,3 +785,61 @@ int mb_timing_end(int cap, int* labels, float* ms, int* n_marks) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-alloc Newton-Schulz
+//
+// For callers that may not allocate device memory: the workspace of
+// mb_newton_schulz lives in this fixed device array instead (one per device
+// that loads the library, held until the process exits).  Calls share it, so
+// calls that overlap on the GPU race; nothing in it needs to start at zero.
+static __device__ __align__(256) unsigned char mb_noalloc_scratch[MB_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the scratch array for the current device, looked up once
+// per device with that device current (the host-side symbol is not a device address).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  MB_TRY_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MB_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    MB_TRY_CUDA(cudaGetSymbolAddress(&p, mb_noalloc_scratch));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MB_OK;
+}
+}  // namespace
+
+extern "C" int mb_newton_schulz_noalloc(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps,
+                                        void* cuda_stream) {
+  MB_TRY(check_shape(shape));
+  MB_TRY(check_ptr(u_bf16));
+  MB_TRY(check_ptr(v_bf16));
+  if (ns_steps < 0 || ns_steps > MAX_NS_STEPS) return MB_ERR_NS_STEPS;
+  const Layout L = make_layout(shape, 0, 0);
+  if (L.end > static_cast<size_t>(MB_NOALLOC_SCRATCH_BYTES)) return MB_ERR_SCRATCH_LIMIT;
+  DeviceState* ds = nullptr;
+  MB_TRY(device_state(&ds));
+  void* scratch = nullptr;
+  MB_TRY(noalloc_scratch(&scratch));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  Bank k{};
+  k.grad = static_cast<const uint16_t*>(u_bf16);
+  k.L = L;
+  k.ws = static_cast<uint8_t*>(scratch);
+  mark(MB_MARK_BEGIN, st);
+  MB_TRY(stage_k1(&k, 1, false, 0.f, st, ds));
+  MB_TRY(stage_ns(&k, 1, ns_steps, st, ds));
+  EwParams p = ew_params(&k, 1, [&](const Bank& bk, EwBank& e) {
+    e.xin = bk.at<uint16_t>(bk.L.x[final_buffer(ns_steps)]);
+    e.xout = static_cast<uint16_t*>(v_bf16);
+    e.out_ld = bk.L.cols;
+  });
+  MB_LAUNCH(launch_unpack(p, st), p.total_blocks > 0, MB_MARK_NS0, st);
+  return MB_OK;
+}
