@@ -319,6 +319,13 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
   int large[MAX_BANKS], nl = 0;
   for (int i = 0; i < nb; ++i)
     if (!b[i].L.small) large[nl++] = i;
+  // longest tiles first: the persistent GEMM CTAs take tiles round-robin in this order
+  for (int i = 1; i < nl; ++i)
+    for (int j = i; j > 0 && b[large[j]].L.n > b[large[j - 1]].L.n; --j) {
+      const int t = large[j];
+      large[j] = large[j - 1];
+      large[j - 1] = t;
+    }
   for (int g0 = 0; g0 < nl; g0 += MAX_GEMM_PROBS) {
     const int gn = (nl - g0 < MAX_GEMM_PROBS) ? nl - g0 : MAX_GEMM_PROBS;
     // tensor maps of this group

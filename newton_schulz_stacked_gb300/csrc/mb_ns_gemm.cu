@@ -15,10 +15,12 @@
 // above the diagonal (paired into 128x256 tiles) and store each off-diagonal
 // block twice, directly and mirrored, so the next phase reads a full matrix.
 //
-// CTA = 6 warps, one output tile of 128 x (128|256) fp32 in TMEM:
+// Persistent CTAs, one per SM, take output tiles of 128 x (128|256) round-robin.
 //   warp 0 lane 0 : TMA producer, STAGES-deep ring of (A 128x64, B 256x64) bf16 tiles
-//   warp 1        : TMEM allocation; lane 0 issues tcgen05.mma (K = 16 per instruction)
-//   warps 2..5    : epilogue, tcgen05.ld of their 32 TMEM lanes, fp32 math, bf16 stores
+//   warp 1        : owns 512 TMEM columns = two 256-column fp32 accumulators;
+//                   lane 0 issues tcgen05.mma (K = 16 per instruction)
+//   warps 2..9    : epilogue, two warps per 32-lane TMEM quadrant (each takes half
+//                   the columns); tile t's epilogue runs under tile t+1's MMAs
 #include "mb_device.cuh"
 #include "mb_internal.h"
 
@@ -33,8 +35,10 @@ constexpr int A_TILE_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_TILE_BYTES = 256 * BK * 2;  // 32 KB
 constexpr int TILE_SMEM = STAGES * (A_TILE_BYTES + B_TILE_BYTES);
 constexpr int GEMM_SMEM = TILE_SMEM + 1024 /* alignment slack */ + 256 /* barriers */;
-constexpr int GEMM_THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr int EPI_WARPS = 8;
+constexpr int GEMM_THREADS = 32 * (2 + EPI_WARPS);
+constexpr uint32_t ACC_COLS = 256;          // one accumulator
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
 struct Tile {
   int pi, mat, m0, n0, nt;
@@ -72,28 +76,32 @@ __device__ __forceinline__ bool decode_tile(const GemmParams& P, int t, Tile& tl
   return false;
 }
 
-// 32 consecutive bf16 of one row -> fp32 (zeros outside [0, ncols) or a masked row).
-__device__ __forceinline__ void load_row32(const uint16_t* base, long long ld, int row, int col0, int ncols,
-                                           bool row_ok, float (&v)[32]) {
+// 32 consecutive bf16 of one row as 16 packed words (zeros outside [0, ncols) or a masked row).
+__device__ __forceinline__ void load_row32_raw(const uint16_t* base, long long ld, int row, int col0, int ncols,
+                                               bool row_ok, uint32_t (&w)[16]) {
   if (row_ok && col0 + 32 <= ncols) {
     const uint4* p = reinterpret_cast<const uint4*>(base + static_cast<long long>(row) * ld + col0);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 w = p[j];
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[8 * j + 2 * i] = bf16_bits_to_float(ws[i] & 0xFFFFu);
-        v[8 * j + 2 * i + 1] = bf16_bits_to_float(ws[i] >> 16);
-      }
+      const uint4 v = p[j];
+      w[4 * j + 0] = v.x;
+      w[4 * j + 1] = v.y;
+      w[4 * j + 2] = v.z;
+      w[4 * j + 3] = v.w;
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      v[i] = (row_ok && col0 + i < ncols) ? bf16_bits_to_float(base[static_cast<long long>(row) * ld + col0 + i])
-                                          : 0.f;
+    for (int i = 0; i < 16; ++i) {
+      uint32_t lo = 0, hi = 0;
+      if (row_ok && col0 + 2 * i < ncols) lo = base[static_cast<long long>(row) * ld + col0 + 2 * i];
+      if (row_ok && col0 + 2 * i + 1 < ncols) hi = base[static_cast<long long>(row) * ld + col0 + 2 * i + 1];
+      w[i] = lo | (hi << 16);
+    }
   }
 }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return bf16_bits_to_float(w & 0xFFFFu); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float(w >> 16); }
 
 __device__ __forceinline__ void store_row32(uint16_t* base, long long ld, int row, int col0, int ncols,
                                             bool row_ok, const float (&o)[32]) {
@@ -112,9 +120,11 @@ __device__ __forceinline__ void store_row32(uint16_t* base, long long ld, int ro
   }
 }
 
+// Epilogue of one warp: TMEM lanes of quadrant `quad` (tile rows quad*32 + lane),
+// columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`.
 template <int EPI>
 __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem& pr, const Tile& tl,
-                                         uint32_t tmem, int quad, int lane) {
+                                         uint32_t tacc, int quad, int half, int lane) {
   const int row = tl.m0 + quad * 32 + lane;
   const bool row_ok = row < pr.M;
   float alpha = 1.f;
@@ -125,26 +135,34 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
   uint16_t* out = pr.out + tl.mat * pr.out_ms;
   const uint16_t* ein = (EPI == EPI_GRAM) ? nullptr : pr.ein + tl.mat * pr.ein_ms;
   const int I = tl.m0 / BM;
+  const int ncols = tl.nt >> 1;
+  const int cbeg = half * ncols;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
 
-  for (int c0 = 0; c0 < tl.nt; c0 += 32) {
+  uint32_t e_cur[16], e_nxt[16];
+  if (EPI != EPI_GRAM) load_row32_raw(ein, pr.ein_ld, row, tl.n0 + cbeg, pr.N, row_ok, e_cur);
+
+  for (int c = 0; c < ncols; c += 32) {
+    const int col0 = tl.n0 + cbeg + c;
+    if (EPI != EPI_GRAM && c + 32 < ncols) load_row32_raw(ein, pr.ein_ld, row, col0 + 32, pr.N, row_ok, e_nxt);
     uint32_t acc[32];
-    tmem_ld_32x32(tmem + lane_base + static_cast<uint32_t>(c0), acc);
+    tmem_ld_32x32(tacc + lane_base + static_cast<uint32_t>(cbeg + c), acc);
     tmem_ld_wait();
-    const int col0 = tl.n0 + c0;
     float o[32];
     if (EPI == EPI_GRAM) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) o[i] = alpha * __uint_as_float(acc[i]);
+    } else if (EPI == EPI_POLY) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[2 * i] = fmaf(P.cc, __uint_as_float(acc[2 * i]), P.cb * bf16_lo(e_cur[i]));
+        o[2 * i + 1] = fmaf(P.cc, __uint_as_float(acc[2 * i + 1]), P.cb * bf16_hi(e_cur[i]));
+      }
     } else {
-      float e[32];
-      load_row32(ein, pr.ein_ld, row, col0, pr.N, row_ok, e);
-      if (EPI == EPI_POLY) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = fmaf(P.cc, __uint_as_float(acc[i]), P.cb * e[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = alpha * fmaf(P.ca, e[i], __uint_as_float(acc[i]));
+      for (int i = 0; i < 16; ++i) {
+        o[2 * i] = alpha * fmaf(P.ca, bf16_lo(e_cur[i]), __uint_as_float(acc[2 * i]));
+        o[2 * i + 1] = alpha * fmaf(P.ca, bf16_hi(e_cur[i]), __uint_as_float(acc[2 * i + 1]));
       }
     }
     if (pr.sym) {
@@ -173,6 +191,10 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
     } else {
       store_row32(out, pr.out_ld, row, col0, pr.N, row_ok, o);
     }
+    if (EPI != EPI_GRAM) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) e_cur[i] = e_nxt[i];
+    }
   }
 }
 
@@ -184,21 +206,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
   uint8_t* sB = smem + STAGES * A_TILE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TILE_SMEM);
   uint64_t* empty = full + STAGES;
-  uint64_t* accf = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  uint64_t* tfull = empty + STAGES;    // [2] accumulator ready for the epilogue
+  uint64_t* tempty = tfull + 2;        // [2] accumulator drained by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Tile tl;
-  const bool valid = decode_tile(P, blockIdx.x, tl);
-  const GemmProblem& pr = P.prob[valid ? tl.pi : 0];
+  const int first = blockIdx.x, stride = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accf, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], EPI_WARPS);
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -211,80 +235,124 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (valid) {
-    const int KB = (pr.K + BK - 1) / BK;
-    if (warp == 0 && lane == 0) {
+  auto fail = [&]() {
+    latch_status(P.status, DEV_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
       // ---------------- TMA producer
-      tma_prefetch_map(&pr.map_a);
-      tma_prefetch_map(&pr.map_b);
-      const uint32_t bytes = A_TILE_BYTES + tl.nt * BK * 2;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % STAGES;
-        if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1)) {
-          latch_status(P.status, DEV_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
-        if (*abort_flag) break;
-        mbar_expect_tx(&full[s], bytes);
-        uint8_t* a = sA + s * A_TILE_BYTES;
-        uint8_t* b = sB + s * B_TILE_BYTES;
-        const int k0 = kb * BK;
-        if (!pr.a_mn) {
-          tma_load_3d(a, &pr.map_a, &full[s], k0, tl.m0, tl.mat);
-        } else {
-          tma_load_3d(a, &pr.map_a, &full[s], tl.m0, k0, tl.mat);
-          tma_load_3d(a + 8192, &pr.map_a, &full[s], tl.m0 + 64, k0, tl.mat);
-        }
-        if (!pr.b_mn) {
-          for (int h = 0; h < tl.nt / 128; ++h)
-            tma_load_3d(b + h * 16384, &pr.map_b, &full[s], k0, tl.n0 + 128 * h, tl.mat);
-        } else {
-          for (int h = 0; h < tl.nt / 64; ++h)
-            tma_load_3d(b + h * 8192, &pr.map_b, &full[s], tl.n0 + 64 * h, k0, tl.mat);
+      for (int pi = 0; pi < P.nprob; ++pi) {
+        tma_prefetch_map(&P.prob[pi].map_a);
+        tma_prefetch_map(&P.prob[pi].map_b);
+      }
+      uint32_t it = 0;
+      for (int t = first; t < P.total_tiles && !*abort_flag; t += stride) {
+        Tile tl;
+        if (!decode_tile(P, t, tl)) break;
+        const GemmProblem& pr = P.prob[tl.pi];
+        const int KB = (pr.K + BK - 1) / BK;
+        const uint32_t bytes = A_TILE_BYTES + tl.nt * BK * 2;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t use = it / STAGES;
+          if (use > 0 && !mbar_wait_or_abort(&empty[s], (use - 1) & 1, abort_flag)) {
+            fail();
+            break;
+          }
+          mbar_expect_tx(&full[s], bytes);
+          uint8_t* a = sA + s * A_TILE_BYTES;
+          uint8_t* b = sB + s * B_TILE_BYTES;
+          const int k0 = kb * BK;
+          if (!pr.a_mn) {
+            tma_load_3d(a, &pr.map_a, &full[s], k0, tl.m0, tl.mat);
+          } else {
+            tma_load_3d(a, &pr.map_a, &full[s], tl.m0, k0, tl.mat);
+            tma_load_3d(a + 8192, &pr.map_a, &full[s], tl.m0 + 64, k0, tl.mat);
+          }
+          if (!pr.b_mn) {
+            for (int h = 0; h < tl.nt / 128; ++h)
+              tma_load_3d(b + h * 16384, &pr.map_b, &full[s], k0, tl.n0 + 128 * h, tl.mat);
+          } else {
+            for (int h = 0; h < tl.nt / 64; ++h)
+              tma_load_3d(b + h * 8192, &pr.map_b, &full[s], tl.n0 + 64 * h, k0, tl.mat);
+          }
         }
       }
-    } else if (warp == 1 && lane == 0) {
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
       // ---------------- MMA issuer
-      const uint32_t idesc = idesc_bf16_m128(tl.nt, pr.a_mn, pr.b_mn);
-      const uint32_t a_step = pr.a_mn ? 2048u : 32u, b_step = pr.b_mn ? 2048u : 32u;
-      const uint32_t a_lbo = pr.a_mn ? 8192u : 16u, b_lbo = pr.b_mn ? 8192u : 16u;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % STAGES;
-        if (!mbar_wait(&full[s], (kb / STAGES) & 1)) {
-          latch_status(P.status, DEV_TIMEOUT);
-          *abort_flag = 1;
+      uint32_t it = 0, j = 0;
+      for (int t = first; t < P.total_tiles && !*abort_flag; t += stride, ++j) {
+        Tile tl;
+        if (!decode_tile(P, t, tl)) break;
+        const GemmProblem& pr = P.prob[tl.pi];
+        const int KB = (pr.K + BK - 1) / BK;
+        const uint32_t buf = j & 1;
+        if (j >= 2 && !mbar_wait_or_abort(&tempty[buf], ((j >> 1) - 1) & 1, abort_flag)) {
+          fail();
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + s * A_TILE_BYTES), b0 = smem_u32(sB + s * B_TILE_BYTES);
+        const uint32_t dacc = tmem + buf * ACC_COLS;
+        const uint32_t idesc = idesc_bf16_m128(tl.nt, pr.a_mn, pr.b_mn);
+        const uint32_t a_step = pr.a_mn ? 2048u : 32u, b_step = pr.b_mn ? 2048u : 32u;
+        const uint32_t a_lbo = pr.a_mn ? 8192u : 16u, b_lbo = pr.b_mn ? 8192u : 16u;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait_or_abort(&full[s], (it / STAGES) & 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * A_TILE_BYTES), b0 = smem_u32(sB + s * B_TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          umma_bf16(tmem, smem_desc_sw128(a0 + kk * a_step, a_lbo, 1024),
-                    smem_desc_sw128(b0 + kk * b_step, b_lbo, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            umma_bf16(dacc, smem_desc_sw128(a0 + kk * a_step, a_lbo, 1024),
+                      smem_desc_sw128(b0 + kk * b_step, b_lbo, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
         }
-        umma_commit(&empty[s]);
+        umma_commit(&tfull[buf]);
+        if (!ok) break;
       }
-      umma_commit(accf);
-    } else if (warp >= 2) {
-      // ---------------- epilogue
-      if (!mbar_wait(accf, 0)) {
-        latch_status(P.status, DEV_TIMEOUT);
-      } else if (!*abort_flag) {
-        tc_fence_after();
-        epilogue<EPI>(P, pr, tl, tmem, warp & 3, lane);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint32_t j = 0;
+    for (int t = first; t < P.total_tiles; t += stride, ++j) {
+      Tile tl;
+      if (!decode_tile(P, t, tl)) break;
+      const uint32_t buf = j & 1;
+      if (!mbar_wait_or_abort(&tfull[buf], (j >> 1) & 1, abort_flag)) {
+        fail();
+        break;
       }
+      if (*abort_flag) break;
+      tc_fence_after();
+      epilogue<EPI>(P, P.prob[tl.pi], tl, tmem + buf * ACC_COLS, quad, half, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
+    tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 bool g_attr_done[3][64];
+int g_num_sms[64];
 
 }  // namespace
 
@@ -293,6 +361,7 @@ cudaError_t launch_gemm(const GemmParams& p, int epi, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const void* fn = nullptr;
   switch (epi) {
     case EPI_GRAM: fn = reinterpret_cast<const void*>(ns_gemm_kernel<EPI_GRAM>); break;
@@ -300,15 +369,20 @@ cudaError_t launch_gemm(const GemmParams& p, int epi, cudaStream_t s) {
     default: fn = reinterpret_cast<const void*>(ns_gemm_kernel<EPI_APPLY>); break;
   }
   const int ei = (epi == EPI_GRAM) ? 0 : (epi == EPI_POLY) ? 1 : 2;
-  if (dev < 64 && !g_attr_done[ei][dev]) {
+  if (!g_attr_done[ei][dev]) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
     if (e != cudaSuccess) return e;
     g_attr_done[ei][dev] = true;
   }
+  if (g_num_sms[dev] == 0) {
+    e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = p.total_tiles < g_num_sms[dev] ? p.total_tiles : g_num_sms[dev];
   switch (epi) {
-    case EPI_GRAM: ns_gemm_kernel<EPI_GRAM><<<p.total_tiles, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
-    case EPI_POLY: ns_gemm_kernel<EPI_POLY><<<p.total_tiles, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
-    default: ns_gemm_kernel<EPI_APPLY><<<p.total_tiles, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
+    case EPI_GRAM: ns_gemm_kernel<EPI_GRAM><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
+    case EPI_POLY: ns_gemm_kernel<EPI_POLY><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
+    default: ns_gemm_kernel<EPI_APPLY><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
   }
   return cudaGetLastError();
 }
