@@ -204,7 +204,7 @@ struct Bank {
 };
 
 int encode_map(CUtensorMap* map, const void* base, int inner, int rows, int batch, int ld, int box_inner,
-               int box_rows) {
+               int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(batch)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
@@ -212,7 +212,7 @@ int encode_map(CUtensorMap* map, const void* base, int inner, int rows, int batc
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     g_last_cuda_error = "cuTensorMapEncodeTiled failed (" + std::to_string(static_cast<int>(r)) + ")";
@@ -331,6 +331,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     // tensor maps of this group
     struct Maps {
       CUtensorMap xk[3], xmn[3], ak, bk;
+      CUtensorMap out_x[3], out_a, out_b;   // 32x32 boxes, no swizzle: epilogue bulk stores
     } maps[MAX_GEMM_PROBS];
     for (int j = 0; j < gn; ++j) {
       const Bank& k = b[large[g0 + j]];
@@ -341,6 +342,11 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
       }
       MB_TRY(encode_map(&maps[j].ak, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 128));
       MB_TRY(encode_map(&maps[j].bk, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 128));
+      for (int t = 1; t < 3; ++t)
+        MB_TRY(encode_map(&maps[j].out_x[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 32, 32,
+                          CU_TENSOR_MAP_SWIZZLE_NONE));
+      MB_TRY(encode_map(&maps[j].out_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
+      MB_TRY(encode_map(&maps[j].out_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
     }
     for (int it = 0; it < steps; ++it) {
       const int cur = iterate_buffer(it), nxt = iterate_buffer(it + 1);
@@ -367,6 +373,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
             pr.M = pr.N = L.m;
             pr.K = L.n;
             pr.sym = 1;
+            pr.map_out = maps[j].out_a;
             pr.out = k.at<uint16_t>(L.a);
             pr.out_ld = L.ldm;
             pr.out_ms = ams;
@@ -377,6 +384,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
             pr.a_mn = pr.b_mn = 0;
             pr.M = pr.N = pr.K = L.m;
             pr.sym = 1;
+            pr.map_out = maps[j].out_b;
             pr.out = k.at<uint16_t>(L.b);
             pr.out_ld = L.ldm;
             pr.out_ms = ams;
@@ -401,6 +409,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
             }
             pr.K = L.m;
             pr.sym = 0;
+            pr.map_out = maps[j].out_x[nxt];
             pr.out = k.at<uint16_t>(L.x[nxt]);
             pr.out_ld = L.ld;
             pr.out_ms = xms;

@@ -92,6 +92,7 @@ enum GemmEpi { EPI_GRAM = 1, EPI_POLY = 2, EPI_APPLY = 3 };
 struct GemmProblem {
   CUtensorMap map_a;     // operand A tiles
   CUtensorMap map_b;     // operand B tiles
+  CUtensorMap map_out;   // output, 32x32 boxes (bulk stores of the epilogue)
   int a_mn, b_mn;        // 0: K-major tiles, 1: MN-major tiles
   int M, N, K;
   int batch;

@@ -34,8 +34,10 @@ constexpr int STAGES = 4;
 constexpr int A_TILE_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_TILE_BYTES = 256 * BK * 2;  // 32 KB
 constexpr int TILE_SMEM = STAGES * (A_TILE_BYTES + B_TILE_BYTES);
-constexpr int GEMM_SMEM = TILE_SMEM + 1024 /* alignment slack */ + 256 /* barriers */;
 constexpr int EPI_WARPS = 8;
+constexpr int EPI_BUF_BYTES = 4096;          // per epilogue warp: 32x32 bf16 chunk + its transpose
+constexpr int EPI_SMEM = EPI_WARPS * EPI_BUF_BYTES;
+constexpr int GEMM_SMEM = TILE_SMEM + EPI_SMEM + 1024 /* alignment slack */ + 256 /* barriers */;
 constexpr int GEMM_THREADS = 32 * (2 + EPI_WARPS);
 constexpr uint32_t ACC_COLS = 256;          // one accumulator
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
@@ -103,36 +105,26 @@ __device__ __forceinline__ void load_row32_raw(const uint16_t* base, long long l
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return bf16_bits_to_float(w & 0xFFFFu); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float(w >> 16); }
 
-__device__ __forceinline__ void store_row32(uint16_t* base, long long ld, int row, int col0, int ncols,
-                                            bool row_ok, const float (&o)[32]) {
-  if (!row_ok) return;
-  if (col0 + 32 <= ncols) {
-    uint4* p = reinterpret_cast<uint4*>(base + static_cast<long long>(row) * ld + col0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      p[j] = make_uint4(pack_bf16x2(o[8 * j + 0], o[8 * j + 1]), pack_bf16x2(o[8 * j + 2], o[8 * j + 3]),
-                        pack_bf16x2(o[8 * j + 4], o[8 * j + 5]), pack_bf16x2(o[8 * j + 6], o[8 * j + 7]));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < ncols)
-        base[static_cast<long long>(row) * ld + col0 + i] = static_cast<uint16_t>(float_to_bf16_bits(o[i]));
-  }
-}
-
 // Epilogue of one warp: TMEM lanes of quadrant `quad` (tile rows quad*32 + lane),
 // columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`.
+// Each 32x32 chunk is staged in the warp's shared buffer and written with a
+// TMA bulk store; a symmetric phase also stores the transposed chunk at the
+// mirrored position.  In a diagonal 128-block the chunks below the diagonal
+// are not stored (their mirror covers them) and the chunk on the diagonal is
+// made symmetric before its store, so every element is written exactly once.
 template <int EPI>
 __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem& pr, const Tile& tl,
-                                         uint32_t tacc, int quad, int half, int lane) {
-  const int row = tl.m0 + quad * 32 + lane;
+                                         uint32_t tacc, int quad, int half, int lane, uint8_t* ebuf) {
+  uint16_t* bufD = reinterpret_cast<uint16_t*>(ebuf);          // [32 rows][32 cols]
+  uint16_t* bufT = reinterpret_cast<uint16_t*>(ebuf + 2048);   // [32 cols][32 rows]
+  const int row0 = tl.m0 + quad * 32;
+  const int row = row0 + lane;
   const bool row_ok = row < pr.M;
   float alpha = 1.f;
   if (pr.scale) {
     const float s = pr.scale[tl.mat];
     alpha = (EPI == EPI_GRAM) ? s * s : s;
   }
-  uint16_t* out = pr.out + tl.mat * pr.out_ms;
   const uint16_t* ein = (EPI == EPI_GRAM) ? nullptr : pr.ein + tl.mat * pr.ein_ms;
   const int I = tl.m0 / BM;
   const int ncols = tl.nt >> 1;
@@ -165,35 +157,66 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
         o[2 * i + 1] = alpha * fmaf(P.ca, bf16_hi(e_cur[i]), __uint_as_float(acc[2 * i + 1]));
       }
     }
-    if (pr.sym) {
-      const int J = col0 / BM;
-      if (J == I) {
-        // diagonal block: the upper half (with the diagonal) directly, the strict upper mirrored
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = col0 + i;
-          if (!row_ok || col >= pr.N) continue;
-          const uint16_t b = static_cast<uint16_t>(float_to_bf16_bits(o[i]));
-          if (col >= row) out[static_cast<long long>(row) * pr.out_ld + col] = b;
-          if (col > row) out[static_cast<long long>(col) * pr.out_ld + row] = b;
-        }
-      } else {
-        store_row32(out, pr.out_ld, row, col0, pr.N, row_ok, o);
-        if (row_ok) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = col0 + i;
-            if (col < pr.N)
-              out[static_cast<long long>(col) * pr.out_ld + row] = static_cast<uint16_t>(float_to_bf16_bits(o[i]));
-          }
-        }
-      }
-    } else {
-      store_row32(out, pr.out_ld, row, col0, pr.N, row_ok, o);
-    }
     if (EPI != EPI_GRAM) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) e_cur[i] = e_nxt[i];
+    }
+
+    // which stores this chunk makes; boxes starting outside the matrix are skipped
+    bool direct = row0 < pr.M && col0 < pr.N, mirror = false, diag = false;
+    if (pr.sym) {
+      const int J = col0 / BM;
+      if (J != I) {
+        mirror = direct;
+      } else {
+        const int cq = (col0 % BM) / 32;
+        if (cq < quad) direct = false;          // below the diagonal: the mirror of (cq, quad) covers it
+        else if (cq > quad) mirror = direct;
+        else diag = direct;
+      }
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+
+    if (lane == 0) bulk_wait_read_all();        // the previous chunk's stores have read the buffers
+    __syncwarp();
+    if (mirror || diag) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        bufT[(2 * i) * 32 + lane] = static_cast<uint16_t>(pk[i] & 0xFFFFu);
+        bufT[(2 * i + 1) * 32 + lane] = static_cast<uint16_t>(pk[i] >> 16);
+      }
+    }
+    if (diag) {
+      __syncwarp();
+      // row `lane` of the symmetric diagonal chunk: own values on and above the
+      // diagonal, the transposed (upper) values below it
+      const uint4* tr = reinterpret_cast<const uint4*>(bufT + lane * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 t4 = tr[j];
+        const uint32_t tw[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c0 = 8 * j + 2 * k;
+          const uint32_t lo = (c0 < lane) ? (tw[k] & 0xFFFFu) : (pk[4 * j + k] & 0xFFFFu);
+          const uint32_t hi = (c0 + 1 < lane) ? (tw[k] >> 16) : (pk[4 * j + k] >> 16);
+          pk[4 * j + k] = lo | (hi << 16);
+        }
+      }
+    }
+    if (direct) {
+      uint4* dr = reinterpret_cast<uint4*>(bufD + lane * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dr[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && (direct || mirror)) {
+      if (direct) tma_store_3d(&pr.map_out, bufD, col0, row0, tl.mat);
+      if (mirror) tma_store_3d(&pr.map_out, bufT, row0, col0, tl.mat);
+      bulk_commit();
     }
   }
 }
@@ -204,7 +227,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_TILE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TILE_SMEM);
+  uint8_t* sEpi = smem + TILE_SMEM;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TILE_SMEM + EPI_SMEM);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;    // [2] accumulator ready for the epilogue
   uint64_t* tempty = tfull + 2;        // [2] accumulator drained by the epilogue
@@ -337,11 +361,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
       }
       if (*abort_flag) break;
       tc_fence_after();
-      epilogue<EPI>(P, P.prob[tl.pi], tl, tmem + buf * ACC_COLS, quad, half, lane);
+      epilogue<EPI>(P, P.prob[tl.pi], tl, tmem + buf * ACC_COLS, quad, half, lane,
+                    sEpi + (warp - 2) * EPI_BUF_BYTES);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
     }
+    if (lane == 0) bulk_wait_all();              // this warp's bulk stores are complete
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
