@@ -287,8 +287,10 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     MB_LAUNCH(launch_ns0(p, st), p.total_blocks > 0, MB_MARK_NS0, st);
     return MB_OK;
   }
-  // small matrices: fp32 SIMT path, one launch
-  {
+  // small matrices: fp32 SIMT path; one launch for those whose iteration fits in
+  // shared memory, one for the rest
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool in_smem = pass == 0;
     SmallParams sp{};
     sp.steps = steps;
     sp.ca = NS_A;
@@ -298,6 +300,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     for (int i = 0; i < nb; ++i) {
       const Layout& L = b[i].L;
       if (!L.small) continue;
+      if ((small_ns_smem_bytes(L.rows, L.cols) <= SMALL_SMEM_MAX) != in_smem) continue;
       SmallBank& s = sp.b[n++];
       s.x0 = b[i].at<uint16_t>(L.x[0]);
       s.xf0 = b[i].at<float>(L.xf[0]);
@@ -313,7 +316,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     }
     sp.nb = n;
     sp.total_blocks = blocks;
-    MB_LAUNCH(launch_small_ns(sp, st), sp.total_blocks > 0, MB_MARK_SMALL_NS, st);
+    MB_LAUNCH(launch_small_ns(sp, in_smem, st), sp.total_blocks > 0, MB_MARK_SMALL_NS, st);
   }
   // large matrices: tcgen05 GEMMs, up to MAX_GEMM_PROBS banks per launch
   int large[MAX_BANKS], nl = 0;
@@ -331,7 +334,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     // tensor maps of this group
     struct Maps {
       CUtensorMap xk[3], xmn[3], ak, bk;
-      CUtensorMap out_x[3], out_a, out_b;   // 32x32 boxes, no swizzle: epilogue bulk stores
+      CUtensorMap out_x[3], out_a, out_b;   // 32x32 boxes, 64-byte swizzle: epilogue bulk stores
     } maps[MAX_GEMM_PROBS];
     for (int j = 0; j < gn; ++j) {
       const Bank& k = b[large[g0 + j]];
@@ -344,9 +347,9 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
       MB_TRY(encode_map(&maps[j].bk, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 128));
       for (int t = 1; t < 3; ++t)
         MB_TRY(encode_map(&maps[j].out_x[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 32, 32,
-                          CU_TENSOR_MAP_SWIZZLE_NONE));
-      MB_TRY(encode_map(&maps[j].out_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
-      MB_TRY(encode_map(&maps[j].out_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
+                          CU_TENSOR_MAP_SWIZZLE_64B));
+      MB_TRY(encode_map(&maps[j].out_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
+      MB_TRY(encode_map(&maps[j].out_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
     }
     for (int it = 0; it < steps; ++it) {
       const int cur = iterate_buffer(it), nxt = iterate_buffer(it + 1);

@@ -168,11 +168,14 @@ __global__ void __launch_bounds__(EW_THREADS) unpack_kernel(const __grid_constan
 
 // ---------------------------------------------------------------- small-matrix NS (fp32)
 
-constexpr int SMALL_THREADS = 256;
+constexpr int SMALL_THREADS = 512;
 
+// One block per matrix.  IN_SMEM: both fp32 copies of X and A, B live in
+// dynamic shared memory (the gate matrices); otherwise X ping-pongs through the
+// fp32 workspace and A, B use the first 2 * SMALL_M^2 floats of shared memory.
+template <bool IN_SMEM>
 __global__ void __launch_bounds__(SMALL_THREADS) small_ns_kernel(const __grid_constant__ SmallParams p) {
-  __shared__ float sA[SMALL_M * SMALL_M];
-  __shared__ float sB[SMALL_M * SMALL_M];
+  extern __shared__ float dsm[];
   int bi = 0;
   while (bi + 1 < p.nb && static_cast<int>(blockIdx.x) >= p.b[bi + 1].block_begin) ++bi;
   const SmallBank& B = p.b[bi];
@@ -180,8 +183,20 @@ __global__ void __launch_bounds__(SMALL_THREADS) small_ns_kernel(const __grid_co
   const int rows = B.rows, cols = B.cols, E = rows * cols;
   const bool tall = rows > cols;
   const int m = tall ? cols : rows;
+  const int n = tall ? rows : cols;
   const size_t moff = static_cast<size_t>(mat) * E;
-  float* xf[2] = {B.xf0 + moff, B.xf1 + moff};
+  float* xf[2];
+  float* sA;
+  if (IN_SMEM) {
+    xf[0] = dsm;
+    xf[1] = dsm + E;
+    sA = dsm + 2 * E;
+  } else {
+    xf[0] = B.xf0 + moff;
+    xf[1] = B.xf1 + moff;
+    sA = dsm;
+  }
+  float* sB = sA + m * m;
   const uint16_t* x0 = B.x0 + static_cast<size_t>(mat) * rows * B.ld;
   const float s = B.scale[mat];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -193,7 +208,6 @@ __global__ void __launch_bounds__(SMALL_THREADS) small_ns_kernel(const __grid_co
   __syncthreads();
 
   // logical X is m x n: X(i, k) = stored(i, k) if wide, stored(k, i) if tall
-  const int n = tall ? rows : cols;
   for (int it = 0; it < p.steps; ++it) {
     const float* cur = xf[it & 1];
     float* nxt = xf[(it + 1) & 1];
@@ -201,7 +215,10 @@ __global__ void __launch_bounds__(SMALL_THREADS) small_ns_kernel(const __grid_co
     const int npairs = m * (m + 1) / 2;
     for (int pr = warp; pr < npairs; pr += SMALL_THREADS / 32) {
       int i = 0, rem = pr;
-      while (rem >= m - i) { rem -= m - i; ++i; }
+      while (rem >= m - i) {
+        rem -= m - i;
+        ++i;
+      }
       const int j = i + rem;
       float acc = 0.f;
       for (int k = lane; k < n; k += 32) {
@@ -429,9 +446,33 @@ cudaError_t launch_unpack(const EwParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_small_ns(const SmallParams& p, cudaStream_t s) {
+int small_ns_smem_bytes(int rows, int cols) {
+  const int m = rows < cols ? rows : cols;
+  return (2 * rows * cols + 2 * m * m) * static_cast<int>(sizeof(float));
+}
+
+cudaError_t launch_small_ns(const SmallParams& p, bool in_smem, cudaStream_t s) {
   if (p.total_blocks == 0) return cudaSuccess;
-  small_ns_kernel<<<p.total_blocks, SMALL_THREADS, 0, s>>>(p);
+  if (!in_smem) {
+    small_ns_kernel<false><<<p.total_blocks, SMALL_THREADS, 2 * SMALL_M * SMALL_M * sizeof(float), s>>>(p);
+    return cudaGetLastError();
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_done[64];
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(small_ns_kernel<true>),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  int bytes = 0;
+  for (int i = 0; i < p.nb; ++i) {
+    const int b = small_ns_smem_bytes(p.b[i].rows, p.b[i].cols);
+    bytes = b > bytes ? b : bytes;
+  }
+  small_ns_kernel<true><<<p.total_blocks, SMALL_THREADS, bytes, s>>>(p);
   return cudaGetLastError();
 }
 

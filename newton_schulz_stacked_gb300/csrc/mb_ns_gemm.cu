@@ -102,6 +102,13 @@ __device__ __forceinline__ void load_row32_raw(const uint16_t* base, long long l
   }
 }
 
+// Byte offset of 16-byte chunk `chunk` of row `row` in a [32][32] bf16 staging
+// buffer laid out as the TMA 64-byte swizzle expects (address bits [4,6) XOR
+// bits [7,9)): row-wise 16-byte writes of a warp then hit distinct banks.
+__device__ __forceinline__ uint32_t sw64(int row, int chunk) {
+  return static_cast<uint32_t>(row * 64 + 16 * (chunk ^ ((row >> 1) & 3)));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return bf16_bits_to_float(w & 0xFFFFu); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float(w >> 16); }
 
@@ -115,8 +122,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float
 template <int EPI>
 __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem& pr, const Tile& tl,
                                          uint32_t tacc, int quad, int half, int lane, uint8_t* ebuf) {
-  uint16_t* bufD = reinterpret_cast<uint16_t*>(ebuf);          // [32 rows][32 cols]
-  uint16_t* bufT = reinterpret_cast<uint16_t*>(ebuf + 2048);   // [32 cols][32 rows]
+  uint8_t* bufD = ebuf;          // [32 rows][32 cols] bf16, 64-byte swizzle
+  uint8_t* bufT = ebuf + 2048;   // [32 cols][32 rows] bf16, 64-byte swizzle
   const int row0 = tl.m0 + quad * 32;
   const int row = row0 + lane;
   const bool row_ok = row < pr.M;
@@ -182,20 +189,20 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
     if (lane == 0) bulk_wait_read_all();        // the previous chunk's stores have read the buffers
     __syncwarp();
     if (mirror || diag) {
+      const uint32_t lane_off = 2u * (lane & 7);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        bufT[(2 * i) * 32 + lane] = static_cast<uint16_t>(pk[i] & 0xFFFFu);
-        bufT[(2 * i + 1) * 32 + lane] = static_cast<uint16_t>(pk[i] >> 16);
+        *reinterpret_cast<uint16_t*>(bufT + sw64(2 * i, lane >> 3) + lane_off) = static_cast<uint16_t>(pk[i] & 0xFFFFu);
+        *reinterpret_cast<uint16_t*>(bufT + sw64(2 * i + 1, lane >> 3) + lane_off) = static_cast<uint16_t>(pk[i] >> 16);
       }
     }
     if (diag) {
       __syncwarp();
       // row `lane` of the symmetric diagonal chunk: own values on and above the
       // diagonal, the transposed (upper) values below it
-      const uint4* tr = reinterpret_cast<const uint4*>(bufT + lane * 32);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 t4 = tr[j];
+        const uint4 t4 = *reinterpret_cast<const uint4*>(bufT + sw64(lane, j));
         const uint32_t tw[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -207,9 +214,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
       }
     }
     if (direct) {
-      uint4* dr = reinterpret_cast<uint4*>(bufD + lane * 32);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) dr[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(bufD + sw64(lane, j)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     }
     fence_proxy_async_smem();
     __syncwarp();

@@ -86,6 +86,8 @@ NS_SHAPES = [
     ((2, 200, 328), "gauss"), ((2, 328, 200), "gauss"), ((2, 65, 130), "gauss"), ((2, 130, 65), "gauss"),
     ((2, 768, 768), "lowrank"), ((1, 768, 3072), "gauss"), ((2, 3072, 768), "lowrank"),
     ((3, 12, 768), "lowrank"), ((3, 6, 12), "lowrank"), ((2, 64, 64), "gauss"), ((2, 1, 40), "gauss"),
+    # small min(rows, cols) whose fp32 iteration does not fit in shared memory: workspace path
+    ((2, 40, 2000), "gauss"), ((2, 1500, 50), "lowrank"),
 ]
 
 
