@@ -312,8 +312,8 @@ def run_native(args):
     # per-stage device time from the library's stage events (same stream, same timed steps)
     tot = timer.totals()
     per = {k: v[0] / args.steps for k, v in tot.items()}
-    gemm_ms = per.get("gram", 0.0) + per.get("poly", 0.0) + per.get("apply", 0.0)
-    gemm_launches = sum(tot.get(k, (0, 0))[1] for k in ("gram", "poly", "apply"))
+    gemm_ms = per.get("ns_gemm", 0.0)
+    gemm_launches = tot.get("ns_gemm", (0, 0))[1]
     fl = ns_flops(shapes, wl.ns_steps)
     E = elems(shapes)
     pk, pk_kind = peaks()
@@ -326,7 +326,8 @@ def run_native(args):
     per_launch_ms = gemm_ms * args.steps / max(gemm_launches, 1)
 
     roofline = {
-        "bound": "tensor", "kernel": "ns_gemm_kernel (A=XX^T, B=bA+cAA, X=aX+BX; %d launches per step)" % (
+        "bound": "tensor",
+        "kernel": "ns_fused_kernel: all Newton-Schulz steps (A=XX^T, B=bA+cAA, X=aX+BX), %d launch(es) per step" % (
             gemm_launches // args.steps),
         "achieved": ns_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
         "frac": (ns_tflops / tensor_peak) if ns_tflops else None,

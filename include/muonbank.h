@@ -196,12 +196,10 @@ enum {
   MB_MARK_MOMENTUM = 1,   /* after S1 (and the u^2 partial sums) */
   MB_MARK_SCALE = 2,      /* after the per-matrix 1/(||u||+eps) */
   MB_MARK_SMALL_NS = 3,   /* after the fp32 Newton-Schulz of small matrices */
-  MB_MARK_GRAM = 4,       /* after one A = X X^T launch */
-  MB_MARK_POLY = 5,       /* after one B = bA + cAA launch */
-  MB_MARK_APPLY = 6,      /* after one X <- aX + BX launch */
-  MB_MARK_NS0 = 7,        /* after the ns_steps = 0 scaling */
-  MB_MARK_ROWSTATS = 8,   /* after the NorMuon row statistics */
-  MB_MARK_UPDATE = 9      /* after S5 */
+  MB_MARK_NS_GEMM = 4,    /* after the tensor-core Newton-Schulz launch (all steps) */
+  MB_MARK_NS0 = 5,        /* after the ns_steps = 0 scaling, or the copy-out of a stage call */
+  MB_MARK_ROWSTATS = 6,   /* after the NorMuon row statistics */
+  MB_MARK_UPDATE = 7      /* after S5 */
 };
 
 /* Starts recording a CUDA event on the launching stream at every stage

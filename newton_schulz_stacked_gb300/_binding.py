@@ -66,8 +66,8 @@ _SIGNATURES = {
     "mb_timing_end": (c_int, [c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_float), ctypes.POINTER(c_int)]),
 }
 
-MARK_NAMES = {0: "begin", 1: "momentum", 2: "scale", 3: "small_ns", 4: "gram", 5: "poly", 6: "apply", 7: "ns0",
-              8: "rowstats", 9: "update"}
+MARK_NAMES = {0: "begin", 1: "momentum", 2: "scale", 3: "small_ns", 4: "ns_gemm", 5: "ns0", 6: "rowstats",
+              7: "update"}
 
 _lib = None
 

@@ -15,7 +15,6 @@ namespace {
 
 // Quintic coefficients ("Muon Custom Sizing" write-up, section 2.3).
 constexpr float NS_A = 3.4445f, NS_B = -4.7750f, NS_C = 2.0315f;
-constexpr int MAX_NS_STEPS = 16;
 constexpr size_t WS_ALIGN = 1024;
 
 __device__ int g_status;  // latched device-side status, one per device
@@ -141,6 +140,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Layout {
   int batch, rows, cols, m, n, tall, small, ld, ldm, P;
   size_t x[3], a, b, xf[2], partials, scale, q, rowscale;  // x[0] = u, x[1], x[2] = iterates
+  size_t sync, sync_bytes;   // large banks: NS completion counters, then the task counter
   size_t end;
 };
 
@@ -169,6 +169,8 @@ Layout make_layout(const mb_shape& s, int normuon, size_t base) {
   if (!L.small) {
     L.a = take(B * L.m * L.ldm * 2);
     L.b = take(B * L.m * L.ldm * 2);
+    L.sync_bytes = B * MAX_NS_STEPS * 3 * sizeof(unsigned) + 16;
+    L.sync = take(L.sync_bytes);
   } else {
     L.xf[0] = take(B * E * 4);
     L.xf[1] = take(B * E * 4);
@@ -318,7 +320,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     sp.total_blocks = blocks;
     MB_LAUNCH(launch_small_ns(sp, in_smem, st), sp.total_blocks > 0, MB_MARK_SMALL_NS, st);
   }
-  // large matrices: tcgen05 GEMMs, up to MAX_GEMM_PROBS banks per launch
+  // large matrices: every step of every bank in one fused tcgen05 launch (up to MAX_NS_BANKS banks each)
   int large[MAX_BANKS], nl = 0;
   for (int i = 0; i < nb; ++i)
     if (!b[i].L.small) large[nl++] = i;
@@ -329,115 +331,68 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
       large[j] = large[j - 1];
       large[j - 1] = t;
     }
-  for (int g0 = 0; g0 < nl; g0 += MAX_GEMM_PROBS) {
-    const int gn = (nl - g0 < MAX_GEMM_PROBS) ? nl - g0 : MAX_GEMM_PROBS;
-    // tensor maps of this group
-    struct Maps {
-      CUtensorMap xk[3], xmn[3], ak, bk;
-      CUtensorMap out_x[3], out_a, out_b;   // 32x32 boxes, 64-byte swizzle: epilogue bulk stores
-    } maps[MAX_GEMM_PROBS];
+  for (int g0 = 0; g0 < nl; g0 += MAX_NS_BANKS) {
+    const int gn = (nl - g0 < MAX_NS_BANKS) ? nl - g0 : MAX_NS_BANKS;
+    NsParams np{};
+    np.nbank = gn;
+    np.steps = steps;
+    np.ca = NS_A;
+    np.cb = NS_B;
+    np.cc = NS_C;
+    np.status = ds->status;
     for (int j = 0; j < gn; ++j) {
       const Bank& k = b[large[g0 + j]];
       const Layout& L = k.L;
+      NsBank& nb_ = np.bank[j];
       for (int t = 0; t < 3; ++t) {
-        MB_TRY(encode_map(&maps[j].xk[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 128));
-        MB_TRY(encode_map(&maps[j].xmn[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 64));
-      }
-      MB_TRY(encode_map(&maps[j].ak, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 128));
-      MB_TRY(encode_map(&maps[j].bk, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 128));
-      for (int t = 1; t < 3; ++t)
-        MB_TRY(encode_map(&maps[j].out_x[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 32, 32,
+        MB_TRY(encode_map(&nb_.xk[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 128));
+        MB_TRY(encode_map(&nb_.xmn[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 64));
+        MB_TRY(encode_map(&nb_.st_x[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 32, 32,
                           CU_TENSOR_MAP_SWIZZLE_64B));
-      MB_TRY(encode_map(&maps[j].out_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
-      MB_TRY(encode_map(&maps[j].out_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
-    }
-    for (int it = 0; it < steps; ++it) {
-      const int cur = iterate_buffer(it), nxt = iterate_buffer(it + 1);
-      for (int phase = EPI_GRAM; phase <= EPI_APPLY; ++phase) {
-        GemmParams gp{};
-        gp.nprob = gn;
-        gp.ca = NS_A;
-        gp.cb = NS_B;
-        gp.cc = NS_C;
-        gp.status = ds->status;
-        int tiles = 0;
-        for (int j = 0; j < gn; ++j) {
-          const Bank& k = b[large[g0 + j]];
-          const Layout& L = k.L;
-          GemmProblem& pr = gp.prob[j];
-          pr.batch = L.batch;
-          const long long xms = static_cast<long long>(L.rows) * L.ld;
-          const long long ams = static_cast<long long>(L.m) * L.ldm;
-          if (phase == EPI_GRAM) {
-            // A = X X^T (wide, K-major tiles of X) or X^T X (tall, MN-major tiles)
-            pr.map_a = L.tall ? maps[j].xmn[cur] : maps[j].xk[cur];
-            pr.map_b = pr.map_a;
-            pr.a_mn = pr.b_mn = L.tall;
-            pr.M = pr.N = L.m;
-            pr.K = L.n;
-            pr.sym = 1;
-            pr.map_out = maps[j].out_a;
-            pr.out = k.at<uint16_t>(L.a);
-            pr.out_ld = L.ldm;
-            pr.out_ms = ams;
-            pr.scale = it == 0 ? k.at<float>(L.scale) : nullptr;
-          } else if (phase == EPI_POLY) {
-            pr.map_a = maps[j].ak;
-            pr.map_b = maps[j].ak;
-            pr.a_mn = pr.b_mn = 0;
-            pr.M = pr.N = pr.K = L.m;
-            pr.sym = 1;
-            pr.map_out = maps[j].out_b;
-            pr.out = k.at<uint16_t>(L.b);
-            pr.out_ld = L.ldm;
-            pr.out_ms = ams;
-            pr.ein = k.at<uint16_t>(L.a);
-            pr.ein_ld = L.ldm;
-            pr.ein_ms = ams;
-          } else {
-            if (!L.tall) {  // X' = a X + B X: B rows K-major, X MN-major
-              pr.map_a = maps[j].bk;
-              pr.map_b = maps[j].xmn[cur];
-              pr.a_mn = 0;
-              pr.b_mn = 1;
-              pr.M = L.m;
-              pr.N = L.n;
-            } else {        // X' = a X + X B: X rows K-major, B rows K-major
-              pr.map_a = maps[j].xk[cur];
-              pr.map_b = maps[j].bk;
-              pr.a_mn = 0;
-              pr.b_mn = 0;
-              pr.M = L.n;
-              pr.N = L.m;
-            }
-            pr.K = L.m;
-            pr.sym = 0;
-            pr.map_out = maps[j].out_x[nxt];
-            pr.out = k.at<uint16_t>(L.x[nxt]);
-            pr.out_ld = L.ld;
-            pr.out_ms = xms;
-            pr.ein = k.at<uint16_t>(L.x[cur]);
-            pr.ein_ld = L.ld;
-            pr.ein_ms = xms;
-            pr.scale = it == 0 ? k.at<float>(L.scale) : nullptr;
-          }
-          if (pr.sym) {
-            pr.T = (pr.M + 127) / 128;
-            int t = 0;
-            for (int I = 0; I < pr.T; ++I) t += (pr.T - I + 1) / 2;
-            pr.tiles_per_mat = t;
-          } else {
-            pr.tn = (pr.N + 255) / 256;
-            pr.tiles_per_mat = ((pr.M + 127) / 128) * pr.tn;
-          }
-          pr.tile_begin = tiles;
-          tiles += pr.batch * pr.tiles_per_mat;
-        }
-        gp.total_tiles = tiles;
-        const int lab = phase == EPI_GRAM ? MB_MARK_GRAM : phase == EPI_POLY ? MB_MARK_POLY : MB_MARK_APPLY;
-        MB_LAUNCH(launch_gemm(gp, phase, st), gp.total_tiles > 0, lab, st);
+        nb_.x[t] = k.at<uint16_t>(L.x[t]);
       }
+      MB_TRY(encode_map(&nb_.ak, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 128));
+      MB_TRY(encode_map(&nb_.bk, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 128));
+      MB_TRY(encode_map(&nb_.st_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
+      MB_TRY(encode_map(&nb_.st_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
+      nb_.a = k.at<uint16_t>(L.a);
+      nb_.x_ld = L.ld;
+      nb_.x_ms = static_cast<long long>(L.rows) * L.ld;
+      nb_.m_ld = L.ldm;
+      nb_.m_ms = static_cast<long long>(L.m) * L.ldm;
+      nb_.scale = k.at<float>(L.scale);
+      nb_.done = k.at<unsigned>(L.sync);
+      nb_.batch = L.batch;
+      nb_.rows = L.rows;
+      nb_.cols = L.cols;
+      nb_.m = L.m;
+      nb_.n = L.n;
+      nb_.tall = L.tall;
+      nb_.T = (L.m + 127) / 128;
+      int t = 0;
+      for (int I = 0; I < nb_.T; ++I) t += (nb_.T - I + 1) / 2;
+      nb_.sym_tiles = t;
+      const int M = L.tall ? L.n : L.m, N = L.tall ? L.m : L.n;
+      nb_.tn = (N + 255) / 256;
+      nb_.apply_tiles = ((M + 127) / 128) * nb_.tn;
+      MB_TRY_CUDA(cudaMemsetAsync(k.ws + L.sync, 0, L.sync_bytes, st));
     }
+    // task numbering inside one step: phase, then bank, then matrix and tile
+    int per_iter = 0;
+    for (int ph = EPI_GRAM; ph <= EPI_APPLY; ++ph) {
+      np.phase_begin[ph] = per_iter;
+      int in_phase = 0;
+      for (int j = 0; j < gn; ++j) {
+        np.bank[j].begin[ph] = in_phase;
+        in_phase += np.bank[j].batch * (ph == EPI_APPLY ? np.bank[j].apply_tiles : np.bank[j].sym_tiles);
+      }
+      per_iter += in_phase;
+    }
+    np.tasks_per_iter = per_iter;
+    np.total_tasks = per_iter * steps;
+    const Bank& first = b[large[g0]];
+    np.next_task = reinterpret_cast<unsigned*>(first.ws + first.L.sync + first.L.sync_bytes - 16);
+    MB_LAUNCH(launch_ns_fused(np, st), np.total_tasks > 0, MB_MARK_NS_GEMM, st);
   }
   return MB_OK;
 }

@@ -9,7 +9,6 @@
 namespace mb {
 
 constexpr int MAX_BANKS = 8;       // banks per element-wise launch
-constexpr int MAX_GEMM_PROBS = 4;  // banks per Newton-Schulz GEMM launch
 constexpr int SMALL_M = 64;        // min(rows, cols) <= SMALL_M: fp32 SIMT Newton-Schulz
 
 // Elements handled by one block of the element-wise kernels (per matrix chunk).
@@ -87,31 +86,35 @@ struct RowParams {
 
 // ---------------------------------------------------------------- Newton-Schulz GEMMs
 
-enum GemmEpi { EPI_GRAM = 1, EPI_POLY = 2, EPI_APPLY = 3 };
+enum GemmEpi { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2 };   // the three GEMM phases of one step
 
-struct GemmProblem {
-  CUtensorMap map_a;     // operand A tiles
-  CUtensorMap map_b;     // operand B tiles
-  CUtensorMap map_out;   // output, 32x32 boxes (bulk stores of the epilogue)
-  int a_mn, b_mn;        // 0: K-major tiles, 1: MN-major tiles
-  int M, N, K;
-  int batch;
-  int sym;               // upper-triangle 128-blocks, mirrored stores
-  int T;                 // sym: 128-blocks per side
-  int tn;                // dense: 256-wide column tiles
-  int tiles_per_mat;
-  int tile_begin;
-  uint16_t* out;         // bf16 output, pitch out_ld, matrix stride out_ms
-  long long out_ld, out_ms;
-  const uint16_t* ein;   // epilogue input (A for POLY, X for APPLY)
-  long long ein_ld, ein_ms;
-  const float* scale;    // per-matrix Frobenius scale (first iteration) or null
+constexpr int MAX_NS_BANKS = 4;     // large banks per fused Newton-Schulz launch
+constexpr int MAX_NS_STEPS = 16;
+
+// One large bank in the fused Newton-Schulz launch.  x[0] holds u; the
+// iterates X_1, X_2, ... alternate between x[1] and x[2].
+struct NsBank {
+  CUtensorMap xk[3];                // X buffers as K-major 128x64 operand tiles
+  CUtensorMap xmn[3];               // the same buffers as MN-major 64x64 operand tiles
+  CUtensorMap ak, bk;               // A and B as K-major operand tiles
+  CUtensorMap st_x[3], st_a, st_b;  // 32x32 store boxes (64-byte swizzle)
+  const uint16_t* x[3];
+  const uint16_t* a;
+  long long x_ld, x_ms, m_ld, m_ms;  // pitches (elements) and matrix strides
+  const float* scale;               // per-matrix 1/(||u||_F + eps)
+  unsigned* done;                   // completion counters [batch][MAX_NS_STEPS][3], zeroed before launch
+  int batch, rows, cols, m, n, tall;
+  int T, sym_tiles;                 // 128-blocks per side of A; tiles per matrix of GRAM and POLY
+  int tn, apply_tiles;              // 256-wide column tiles and tiles per matrix of APPLY
+  int begin[3];                     // first task of this bank within each phase of one iteration
 };
 
-struct GemmParams {
-  GemmProblem prob[MAX_GEMM_PROBS];
-  int nprob;
-  int total_tiles;
+struct NsParams {
+  NsBank bank[MAX_NS_BANKS];
+  int nbank, steps;
+  int phase_begin[3];               // first task of each phase within one iteration
+  int tasks_per_iter, total_tasks;
+  unsigned* next_task;              // dynamic scheduler, zeroed before launch
   float ca, cb, cc;
   int* status;
 };
@@ -131,6 +134,6 @@ cudaError_t launch_row_sumsq(const RowParams& p, cudaStream_t s);
 cudaError_t launch_row_scale(const RowParams& p, cudaStream_t s);
 cudaError_t launch_k3(const EwParams& p, bool normuon, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
-cudaError_t launch_gemm(const GemmParams& p, int epi, cudaStream_t s);
+cudaError_t launch_ns_fused(const NsParams& p, cudaStream_t s);
 
 }  // namespace mb

@@ -1,26 +1,37 @@
-// Batched Newton-Schulz GEMMs on the sm_103a tensor cores (tcgen05 + TMEM,
-// operands staged by TMA with 128-byte swizzle).
+// Batched Newton-Schulz iteration on the sm_103a tensor cores (tcgen05 + TMEM,
+// operands staged by TMA with 128-byte swizzle), all steps in one launch.
 //
 // One quintic step ("Muon Custom Sizing" write-up, section 2.3; Track-2
-// record 7 write-up, section 4.2) is three GEMM phases over every matrix of
-// the bank(s) in the launch:
-//   EPI_GRAM   A  = alpha * X X^T       (alpha = s^2 on the first step, s = 1/(||u||+eps))
-//   EPI_POLY   B  = b A + c A A         (A symmetric, so A A = A A^T)
-//   EPI_APPLY  X' = beta (a X + B X)    (beta = s on the first step)
+// record 7 write-up, section 4.2) is three GEMM phases per matrix:
+//   GRAM   A  = alpha * X X^T       (alpha = s^2 on the first step, s = 1/(||u||+eps))
+//   POLY   B  = b A + c A A         (A symmetric, so A A = A A^T)
+//   APPLY  X' = beta (a X + B X)    (beta = s on the first step)
 // A tall slice (rows > cols) stays in its stored orientation and runs the
 // swapped-operand form A = X^T X, X' = beta (a X + X B); the difference is
 // only which operand tiles are K-major and which are MN-major.
 //
-// A and B are symmetric: those phases compute only the 128x128 blocks on or
+// A and B are symmetric: GRAM and POLY compute only the 128x128 blocks on or
 // above the diagonal (paired into 128x256 tiles) and store each off-diagonal
 // block twice, directly and mirrored, so the next phase reads a full matrix.
 //
-// Persistent CTAs, one per SM, take output tiles of 128 x (128|256) round-robin.
-//   warp 0 lane 0 : TMA producer, STAGES-deep ring of (A 128x64, B 256x64) bf16 tiles
+// Scheduling.  The work of all steps is one list of tasks (an output tile of
+// one phase of one matrix), ordered by step, then phase, then bank, matrix
+// and tile.  Persistent CTAs, one per SM, claim tasks in that order from a
+// global counter.  A task's producer first waits until every tile of the
+// previous phase of the same matrix has been stored (per-matrix completion
+// counters, release/acquire at GPU scope), so phases overlap across matrices
+// and there is no launch boundary between them.  Every task depends only on
+// earlier tasks and all CTAs are resident, so the earliest unfinished task
+// can always run; each wait is bounded all the same.
+//
+// CTA roles (10 warps):
+//   warp 0 lane 0 : claims tasks, waits for their inputs, TMA producer of a
+//                   STAGES-deep ring of (A 128x64, B 256x64) bf16 tiles
 //   warp 1        : owns 512 TMEM columns = two 256-column fp32 accumulators;
 //                   lane 0 issues tcgen05.mma (K = 16 per instruction)
-//   warps 2..9    : epilogue, two warps per 32-lane TMEM quadrant (each takes half
-//                   the columns); tile t's epilogue runs under tile t+1's MMAs
+//   warps 2..9    : epilogue, two warps per 32-lane TMEM quadrant (each takes
+//                   half the columns); task k's epilogue runs under task k+1's
+//                   MMAs; results leave through shared memory by TMA bulk stores
 #include "mb_device.cuh"
 #include "mb_internal.h"
 
@@ -37,46 +48,143 @@ constexpr int TILE_SMEM = STAGES * (A_TILE_BYTES + B_TILE_BYTES);
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_BUF_BYTES = 4096;          // per epilogue warp: 32x32 bf16 chunk + its transpose
 constexpr int EPI_SMEM = EPI_WARPS * EPI_BUF_BYTES;
-constexpr int GEMM_SMEM = TILE_SMEM + EPI_SMEM + 1024 /* alignment slack */ + 256 /* barriers */;
+constexpr int TASK_SLOTS = 4;                // claimed tasks in flight inside a CTA
+constexpr int GEMM_SMEM = TILE_SMEM + EPI_SMEM + 1024 /* alignment slack */ + 512 /* barriers, slots */;
 constexpr int GEMM_THREADS = 32 * (2 + EPI_WARPS);
 constexpr uint32_t ACC_COLS = 256;          // one accumulator
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
-struct Tile {
-  int pi, mat, m0, n0, nt;
+// ---------------------------------------------------------------- tasks
+
+struct Task {
+  int it, ph, bi, mat;   // step, phase, bank, matrix
+  int m0, n0, nt;        // output tile origin and width (128 or 256)
 };
 
-__device__ __forceinline__ bool decode_tile(const GemmParams& P, int t, Tile& tl) {
-  for (int pi = 0; pi < P.nprob; ++pi) {
-    const GemmProblem& pr = P.prob[pi];
-    const int cnt = pr.batch * pr.tiles_per_mat;
-    if (t >= pr.tile_begin + cnt) continue;
-    int lt = t - pr.tile_begin;
-    tl.pi = pi;
-    tl.mat = lt / pr.tiles_per_mat;
-    lt -= tl.mat * pr.tiles_per_mat;
-    if (pr.sym) {
-      for (int I = 0; I < pr.T; ++I) {
-        const int c = (pr.T - I + 1) >> 1;
-        if (lt < c) {
-          const int J = I + 2 * lt;
-          tl.m0 = I * BM;
-          tl.n0 = J * BM;
-          tl.nt = (J + 1 < pr.T) ? 256 : 128;
-          return true;
-        }
-        lt -= c;
+__device__ __forceinline__ int iterate_buffer(int k) { return k == 0 ? 0 : 1 + ((k - 1) & 1); }
+
+__device__ __forceinline__ void decode_task(const NsParams& P, int t, Task& k) {
+  k.it = t / P.tasks_per_iter;
+  int r = t - k.it * P.tasks_per_iter;
+  k.ph = (r >= P.phase_begin[EPI_APPLY]) ? EPI_APPLY : (r >= P.phase_begin[EPI_POLY]) ? EPI_POLY : EPI_GRAM;
+  r -= P.phase_begin[k.ph];
+  int bi = 0;
+  while (bi + 1 < P.nbank && r >= P.bank[bi + 1].begin[k.ph]) ++bi;
+  k.bi = bi;
+  const NsBank& B = P.bank[bi];
+  r -= B.begin[k.ph];
+  k.m0 = k.n0 = 0;
+  k.nt = 128;
+  if (k.ph != EPI_APPLY) {
+    k.mat = r / B.sym_tiles;
+    r -= k.mat * B.sym_tiles;
+    for (int I = 0; I < B.T; ++I) {
+      const int c = (B.T - I + 1) >> 1;
+      if (r < c) {
+        const int J = I + 2 * r;
+        k.m0 = I * BM;
+        k.n0 = J * BM;
+        k.nt = (J + 1 < B.T) ? 256 : 128;
+        return;
       }
-      return false;
+      r -= c;
     }
-    const int tm = lt / pr.tn, tj = lt - tm * pr.tn;
-    tl.m0 = tm * BM;
-    tl.n0 = tj * 256;
-    tl.nt = (pr.N - tl.n0 > 128) ? 256 : 128;
-    return true;
+  } else {
+    k.mat = r / B.apply_tiles;
+    r -= k.mat * B.apply_tiles;
+    const int tm = r / B.tn, tj = r - tm * B.tn;
+    const int N = B.tall ? B.m : B.n;
+    k.m0 = tm * BM;
+    k.n0 = tj * 256;
+    k.nt = (N - k.n0 > 128) ? 256 : 128;
   }
-  return false;
 }
+
+__device__ __forceinline__ int phase_tiles(const NsBank& B, int ph) {
+  return ph == EPI_APPLY ? B.apply_tiles : B.sym_tiles;
+}
+
+__device__ __forceinline__ unsigned* done_counter(const NsBank& B, int mat, int it, int ph) {
+  return B.done + (static_cast<size_t>(mat) * MAX_NS_STEPS + it) * 3 + ph;
+}
+
+// Operands of a task's GEMM.
+struct Operands {
+  const CUtensorMap* a;
+  const CUtensorMap* b;
+  int a_mn, b_mn, K;
+};
+
+__device__ __forceinline__ Operands task_operands(const NsBank& B, const Task& k) {
+  const int cur = iterate_buffer(k.it);
+  Operands o;
+  if (k.ph == EPI_GRAM) {
+    o.a = o.b = B.tall ? &B.xmn[cur] : &B.xk[cur];
+    o.a_mn = o.b_mn = B.tall;
+    o.K = B.n;
+  } else if (k.ph == EPI_POLY) {
+    o.a = o.b = &B.ak;
+    o.a_mn = o.b_mn = 0;
+    o.K = B.m;
+  } else {
+    if (!B.tall) {       // X' = a X + B X: rows of B (K-major), X as MN-major tiles
+      o.a = &B.bk;
+      o.b = &B.xmn[cur];
+      o.a_mn = 0;
+      o.b_mn = 1;
+    } else {             // X' = a X + X B: rows of X and of B, both K-major
+      o.a = &B.xk[cur];
+      o.b = &B.bk;
+      o.a_mn = 0;
+      o.b_mn = 0;
+    }
+    o.K = B.m;
+  }
+  return o;
+}
+
+// ---------------------------------------------------------------- cross-CTA completion
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy view of global memory with its async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits (bounded) until *ctr >= target.
+__device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned target, const volatile int* abort) {
+  if (ld_acquire(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(128);
+    if (ld_acquire(ctr) >= target) return true;
+    if ((i & 15u) == 0u && (*abort || globaltimer_ns() - t0 > WAIT_LIMIT_NS)) return false;
+  }
+}
+
+// The phase a task reads from; false when it reads only the step's input u.
+__device__ __forceinline__ bool dependency(const Task& k, int& dit, int& dph) {
+  if (k.ph == EPI_GRAM) {
+    if (k.it == 0) return false;
+    dit = k.it - 1;
+    dph = EPI_APPLY;
+  } else {
+    dit = k.it;
+    dph = k.ph - 1;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- epilogue
 
 // 32 consecutive bf16 of one row as 16 packed words (zeros outside [0, ncols) or a masked row).
 __device__ __forceinline__ void load_row32_raw(const uint16_t* base, long long ld, int row, int col0, int ncols,
@@ -112,6 +220,14 @@ __device__ __forceinline__ uint32_t sw64(int row, int chunk) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return bf16_bits_to_float(w & 0xFFFFu); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float(w >> 16); }
 
+struct EpiJob {
+  const CUtensorMap* st;   // store map of the output
+  const uint16_t* ein;     // epilogue input of this matrix (A for POLY, X for APPLY)
+  long long ein_ld;
+  int M, N, sym, mat, m0, n0, nt;
+  float alpha;
+};
+
 // Epilogue of one warp: TMEM lanes of quadrant `quad` (tile rows quad*32 + lane),
 // columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`.
 // Each 32x32 chunk is staged in the warp's shared buffer and written with a
@@ -120,37 +236,31 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float
 // are not stored (their mirror covers them) and the chunk on the diagonal is
 // made symmetric before its store, so every element is written exactly once.
 template <int EPI>
-__device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem& pr, const Tile& tl,
-                                         uint32_t tacc, int quad, int half, int lane, uint8_t* ebuf) {
+__device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uint32_t tacc, int quad, int half,
+                                         int lane, uint8_t* ebuf) {
   uint8_t* bufD = ebuf;          // [32 rows][32 cols] bf16, 64-byte swizzle
   uint8_t* bufT = ebuf + 2048;   // [32 cols][32 rows] bf16, 64-byte swizzle
-  const int row0 = tl.m0 + quad * 32;
+  const int row0 = J.m0 + quad * 32;
   const int row = row0 + lane;
-  const bool row_ok = row < pr.M;
-  float alpha = 1.f;
-  if (pr.scale) {
-    const float s = pr.scale[tl.mat];
-    alpha = (EPI == EPI_GRAM) ? s * s : s;
-  }
-  const uint16_t* ein = (EPI == EPI_GRAM) ? nullptr : pr.ein + tl.mat * pr.ein_ms;
-  const int I = tl.m0 / BM;
-  const int ncols = tl.nt >> 1;
+  const bool row_ok = row < J.M;
+  const int I = J.m0 / BM;
+  const int ncols = J.nt >> 1;
   const int cbeg = half * ncols;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
 
   uint32_t e_cur[16], e_nxt[16];
-  if (EPI != EPI_GRAM) load_row32_raw(ein, pr.ein_ld, row, tl.n0 + cbeg, pr.N, row_ok, e_cur);
+  if (EPI != EPI_GRAM) load_row32_raw(J.ein, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, e_cur);
 
   for (int c = 0; c < ncols; c += 32) {
-    const int col0 = tl.n0 + cbeg + c;
-    if (EPI != EPI_GRAM && c + 32 < ncols) load_row32_raw(ein, pr.ein_ld, row, col0 + 32, pr.N, row_ok, e_nxt);
+    const int col0 = J.n0 + cbeg + c;
+    if (EPI != EPI_GRAM && c + 32 < ncols) load_row32_raw(J.ein, J.ein_ld, row, col0 + 32, J.N, row_ok, e_nxt);
     uint32_t acc[32];
     tmem_ld_32x32(tacc + lane_base + static_cast<uint32_t>(cbeg + c), acc);
     tmem_ld_wait();
     float o[32];
     if (EPI == EPI_GRAM) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = alpha * __uint_as_float(acc[i]);
+      for (int i = 0; i < 32; ++i) o[i] = J.alpha * __uint_as_float(acc[i]);
     } else if (EPI == EPI_POLY) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -160,8 +270,8 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        o[2 * i] = alpha * fmaf(P.ca, bf16_lo(e_cur[i]), __uint_as_float(acc[2 * i]));
-        o[2 * i + 1] = alpha * fmaf(P.ca, bf16_hi(e_cur[i]), __uint_as_float(acc[2 * i + 1]));
+        o[2 * i] = J.alpha * fmaf(P.ca, bf16_lo(e_cur[i]), __uint_as_float(acc[2 * i]));
+        o[2 * i + 1] = J.alpha * fmaf(P.ca, bf16_hi(e_cur[i]), __uint_as_float(acc[2 * i + 1]));
       }
     }
     if (EPI != EPI_GRAM) {
@@ -170,10 +280,10 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
     }
 
     // which stores this chunk makes; boxes starting outside the matrix are skipped
-    bool direct = row0 < pr.M && col0 < pr.N, mirror = false, diag = false;
-    if (pr.sym) {
-      const int J = col0 / BM;
-      if (J != I) {
+    bool direct = row0 < J.M && col0 < J.N, mirror = false, diag = false;
+    if (J.sym) {
+      const int Jb = col0 / BM;
+      if (Jb != I) {
         mirror = direct;
       } else {
         const int cq = (col0 % BM) / 32;
@@ -205,11 +315,11 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
         const uint4 t4 = *reinterpret_cast<const uint4*>(bufT + sw64(lane, j));
         const uint32_t tw[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c0 = 8 * j + 2 * k;
-          const uint32_t lo = (c0 < lane) ? (tw[k] & 0xFFFFu) : (pk[4 * j + k] & 0xFFFFu);
-          const uint32_t hi = (c0 + 1 < lane) ? (tw[k] >> 16) : (pk[4 * j + k] >> 16);
-          pk[4 * j + k] = lo | (hi << 16);
+        for (int q = 0; q < 4; ++q) {
+          const int c0 = 8 * j + 2 * q;
+          const uint32_t lo = (c0 < lane) ? (tw[q] & 0xFFFFu) : (pk[4 * j + q] & 0xFFFFu);
+          const uint32_t hi = (c0 + 1 < lane) ? (tw[q] >> 16) : (pk[4 * j + q] >> 16);
+          pk[4 * j + q] = lo | (hi << 16);
         }
       }
     }
@@ -221,15 +331,16 @@ __device__ __forceinline__ void epilogue(const GemmParams& P, const GemmProblem&
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && (direct || mirror)) {
-      if (direct) tma_store_3d(&pr.map_out, bufD, col0, row0, tl.mat);
-      if (mirror) tma_store_3d(&pr.map_out, bufT, row0, col0, tl.mat);
+      if (direct) tma_store_3d(J.st, bufD, col0, row0, J.mat);
+      if (mirror) tma_store_3d(J.st, bufT, row0, col0, J.mat);
       bulk_commit();
     }
   }
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_constant__ GemmParams P) {
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_constant__ NsParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -237,13 +348,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
   uint8_t* sEpi = smem + TILE_SMEM;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TILE_SMEM + EPI_SMEM);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;    // [2] accumulator ready for the epilogue
-  uint64_t* tempty = tfull + 2;        // [2] accumulator drained by the epilogue
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tfull = empty + STAGES;               // [2] accumulator ready for the epilogue
+  uint64_t* tempty = tfull + 2;                   // [2] accumulator drained by the epilogue
+  uint64_t* slot_full = tempty + 2;               // [TASK_SLOTS] claimed task id written
+  uint64_t* slot_empty = slot_full + TASK_SLOTS;  // [TASK_SLOTS] every epilogue warp has read it
+  volatile int* slot = reinterpret_cast<volatile int*>(slot_empty + TASK_SLOTS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(slot + TASK_SLOTS));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int first = blockIdx.x, stride = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -253,6 +366,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], EPI_WARPS);
+    }
+    for (int s = 0; s < TASK_SLOTS; ++s) {
+      mbar_init(&slot_full[s], 1);
+      mbar_init(&slot_empty[s], EPI_WARPS);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -273,41 +390,58 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
-      for (int pi = 0; pi < P.nprob; ++pi) {
-        tma_prefetch_map(&P.prob[pi].map_a);
-        tma_prefetch_map(&P.prob[pi].map_b);
+      // ---------------- task claims + TMA producer
+      for (int b = 0; b < P.nbank; ++b) {
+        tma_prefetch_map(&P.bank[b].ak);
+        tma_prefetch_map(&P.bank[b].bk);
       }
       uint32_t it = 0;
-      for (int t = first; t < P.total_tiles && !*abort_flag; t += stride) {
-        Tile tl;
-        if (!decode_tile(P, t, tl)) break;
-        const GemmProblem& pr = P.prob[tl.pi];
-        const int KB = (pr.K + BK - 1) / BK;
-        const uint32_t bytes = A_TILE_BYTES + tl.nt * BK * 2;
+      for (uint32_t k = 0;; ++k) {
+        const int s = k % TASK_SLOTS;
+        if (k >= TASK_SLOTS && !mbar_wait_or_abort(&slot_empty[s], ((k / TASK_SLOTS) - 1) & 1, abort_flag)) fail();
+        int t = *abort_flag ? -1 : static_cast<int>(atomicAdd(P.next_task, 1u));
+        if (t >= P.total_tasks) t = -1;
+        slot[s] = t;
+        mbar_arrive(&slot_full[s]);
+        if (t < 0) break;
+        Task tk;
+        decode_task(P, t, tk);
+        const NsBank& B = P.bank[tk.bi];
+        int dit, dph;
+        if (dependency(tk, dit, dph)) {
+          const unsigned target = static_cast<unsigned>(phase_tiles(B, dph) * EPI_WARPS);
+          if (!wait_counter(done_counter(B, tk.mat, dit, dph), target, abort_flag)) {
+            fail();
+            continue;   // the slot is published; the consumers see the abort and stop
+          }
+          fence_proxy_async_global();
+        }
+        const Operands op = task_operands(B, tk);
+        const int KB = (op.K + BK - 1) / BK;
+        const uint32_t bytes = A_TILE_BYTES + tk.nt * BK * 2;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % STAGES;
+          const int st = it % STAGES;
           const uint32_t use = it / STAGES;
-          if (use > 0 && !mbar_wait_or_abort(&empty[s], (use - 1) & 1, abort_flag)) {
+          if (use > 0 && !mbar_wait_or_abort(&empty[st], (use - 1) & 1, abort_flag)) {
             fail();
             break;
           }
-          mbar_expect_tx(&full[s], bytes);
-          uint8_t* a = sA + s * A_TILE_BYTES;
-          uint8_t* b = sB + s * B_TILE_BYTES;
+          mbar_expect_tx(&full[st], bytes);
+          uint8_t* a = sA + st * A_TILE_BYTES;
+          uint8_t* b = sB + st * B_TILE_BYTES;
           const int k0 = kb * BK;
-          if (!pr.a_mn) {
-            tma_load_3d(a, &pr.map_a, &full[s], k0, tl.m0, tl.mat);
+          if (!op.a_mn) {
+            tma_load_3d(a, op.a, &full[st], k0, tk.m0, tk.mat);
           } else {
-            tma_load_3d(a, &pr.map_a, &full[s], tl.m0, k0, tl.mat);
-            tma_load_3d(a + 8192, &pr.map_a, &full[s], tl.m0 + 64, k0, tl.mat);
+            tma_load_3d(a, op.a, &full[st], tk.m0, k0, tk.mat);
+            tma_load_3d(a + 8192, op.a, &full[st], tk.m0 + 64, k0, tk.mat);
           }
-          if (!pr.b_mn) {
-            for (int h = 0; h < tl.nt / 128; ++h)
-              tma_load_3d(b + h * 16384, &pr.map_b, &full[s], k0, tl.n0 + 128 * h, tl.mat);
+          if (!op.b_mn) {
+            for (int h = 0; h < tk.nt / 128; ++h)
+              tma_load_3d(b + h * 16384, op.b, &full[st], k0, tk.n0 + 128 * h, tk.mat);
           } else {
-            for (int h = 0; h < tl.nt / 64; ++h)
-              tma_load_3d(b + h * 8192, &pr.map_b, &full[s], tl.n0 + 64 * h, k0, tl.mat);
+            for (int h = 0; h < tk.nt / 64; ++h)
+              tma_load_3d(b + h * 8192, op.b, &full[st], tk.n0 + 64 * h, k0, tk.mat);
           }
         }
       }
@@ -315,38 +449,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      uint32_t it = 0, j = 0;
-      for (int t = first; t < P.total_tiles && !*abort_flag; t += stride, ++j) {
-        Tile tl;
-        if (!decode_tile(P, t, tl)) break;
-        const GemmProblem& pr = P.prob[tl.pi];
-        const int KB = (pr.K + BK - 1) / BK;
-        const uint32_t buf = j & 1;
-        if (j >= 2 && !mbar_wait_or_abort(&tempty[buf], ((j >> 1) - 1) & 1, abort_flag)) {
+      uint32_t it = 0;
+      for (uint32_t k = 0;; ++k) {
+        const int s = k % TASK_SLOTS;
+        if (!mbar_wait_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        const int t = slot[s];
+        if (t < 0 || *abort_flag) break;
+        Task tk;
+        decode_task(P, t, tk);
+        const Operands op = task_operands(P.bank[tk.bi], tk);
+        const int KB = (op.K + BK - 1) / BK;
+        const uint32_t buf = k & 1;
+        if (k >= 2 && !mbar_wait_or_abort(&tempty[buf], ((k >> 1) - 1) & 1, abort_flag)) {
           fail();
           break;
         }
         tc_fence_after();
         const uint32_t dacc = tmem + buf * ACC_COLS;
-        const uint32_t idesc = idesc_bf16_m128(tl.nt, pr.a_mn, pr.b_mn);
-        const uint32_t a_step = pr.a_mn ? 2048u : 32u, b_step = pr.b_mn ? 2048u : 32u;
-        const uint32_t a_lbo = pr.a_mn ? 8192u : 16u, b_lbo = pr.b_mn ? 8192u : 16u;
+        const uint32_t idesc = idesc_bf16_m128(tk.nt, op.a_mn, op.b_mn);
+        const uint32_t a_step = op.a_mn ? 2048u : 32u, b_step = op.b_mn ? 2048u : 32u;
+        const uint32_t a_lbo = op.a_mn ? 8192u : 16u, b_lbo = op.b_mn ? 8192u : 16u;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % STAGES;
-          if (!mbar_wait_or_abort(&full[s], (it / STAGES) & 1, abort_flag)) {
+          const int st = it % STAGES;
+          if (!mbar_wait_or_abort(&full[st], (it / STAGES) & 1, abort_flag)) {
             fail();
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * A_TILE_BYTES), b0 = smem_u32(sB + s * B_TILE_BYTES);
+          const uint32_t a0 = smem_u32(sA + st * A_TILE_BYTES), b0 = smem_u32(sB + st * B_TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             umma_bf16(dacc, smem_desc_sw128(a0 + kk * a_step, a_lbo, 1024),
                       smem_desc_sw128(b0 + kk * b_step, b_lbo, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[s]);
+          umma_commit(&empty[st]);
         }
         umma_commit(&tfull[buf]);
         if (!ok) break;
@@ -357,24 +498,80 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
     // ---------------- epilogue warps
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
-    uint32_t j = 0;
-    for (int t = first; t < P.total_tiles; t += stride, ++j) {
-      Tile tl;
-      if (!decode_tile(P, t, tl)) break;
-      const uint32_t buf = j & 1;
-      if (!mbar_wait_or_abort(&tfull[buf], (j >> 1) & 1, abort_flag)) {
+    uint8_t* ebuf = sEpi + (warp - 2) * EPI_BUF_BYTES;
+    for (uint32_t k = 0;; ++k) {
+      const int s = k % TASK_SLOTS;
+      if (!mbar_wait_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      const int t = slot[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&slot_empty[s]);
+      if (t < 0) break;
+      Task tk;
+      decode_task(P, t, tk);
+      const NsBank& B = P.bank[tk.bi];
+      const uint32_t buf = k & 1;
+      if (!mbar_wait_or_abort(&tfull[buf], (k >> 1) & 1, abort_flag)) {
         fail();
         break;
       }
       if (*abort_flag) break;
       tc_fence_after();
-      epilogue<EPI>(P, P.prob[tl.pi], tl, tmem + buf * ACC_COLS, quad, half, lane,
-                    sEpi + (warp - 2) * EPI_BUF_BYTES);
+      // make the epilogue inputs visible to this warp: A (POLY reads what GRAM wrote) and
+      // X (APPLY reads the previous step's APPLY output)
+      int dit, dph;
+      if (dependency(tk, dit, dph)) ld_acquire(done_counter(B, tk.mat, dit, dph));
+      if (tk.ph == EPI_APPLY && tk.it > 0) ld_acquire(done_counter(B, tk.mat, tk.it - 1, EPI_APPLY));
+      EpiJob J;
+      J.mat = tk.mat;
+      J.m0 = tk.m0;
+      J.n0 = tk.n0;
+      J.nt = tk.nt;
+      J.alpha = 1.f;
+      const uint32_t tacc = tmem + buf * ACC_COLS;
+      if (tk.ph == EPI_GRAM) {
+        if (tk.it == 0) {
+          const float sc = B.scale[tk.mat];
+          J.alpha = sc * sc;
+        }
+        J.st = &B.st_a;
+        J.ein = nullptr;
+        J.ein_ld = 0;
+        J.M = J.N = B.m;
+        J.sym = 1;
+        epilogue<EPI_GRAM>(P, J, tacc, quad, half, lane, ebuf);
+      } else if (tk.ph == EPI_POLY) {
+        J.st = &B.st_b;
+        J.ein = B.a + tk.mat * B.m_ms;
+        J.ein_ld = B.m_ld;
+        J.M = J.N = B.m;
+        J.sym = 1;
+        epilogue<EPI_POLY>(P, J, tacc, quad, half, lane, ebuf);
+      } else {
+        if (tk.it == 0) J.alpha = B.scale[tk.mat];
+        J.st = &B.st_x[iterate_buffer(tk.it + 1)];
+        J.ein = B.x[iterate_buffer(tk.it)] + tk.mat * B.x_ms;
+        J.ein_ld = B.x_ld;
+        J.M = B.tall ? B.n : B.m;
+        J.N = B.tall ? B.m : B.n;
+        J.sym = 0;
+        epilogue<EPI_APPLY>(P, J, tacc, quad, half, lane, ebuf);
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (lane == 0) {
+        mbar_arrive(&tempty[buf]);
+        // publish: this warp's part of the tile is in global memory
+        bulk_wait_all();
+        fence_proxy_async_global();
+        __threadfence();
+        red_release_add(done_counter(B, tk.mat, tk.it, tk.ph), 1u);
+      }
+      __syncwarp();
     }
-    if (lane == 0) bulk_wait_all();              // this warp's bulk stores are complete
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
   tc_fence_before();
@@ -385,39 +582,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_gemm_kernel(const __grid_c
   }
 }
 
-bool g_attr_done[3][64];
+bool g_attr_done[64];
 int g_num_sms[64];
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmParams& p, int epi, cudaStream_t s) {
-  if (p.total_tiles == 0) return cudaSuccess;
+cudaError_t launch_ns_fused(const NsParams& p, cudaStream_t s) {
+  if (p.total_tasks == 0) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const void* fn = nullptr;
-  switch (epi) {
-    case EPI_GRAM: fn = reinterpret_cast<const void*>(ns_gemm_kernel<EPI_GRAM>); break;
-    case EPI_POLY: fn = reinterpret_cast<const void*>(ns_gemm_kernel<EPI_POLY>); break;
-    default: fn = reinterpret_cast<const void*>(ns_gemm_kernel<EPI_APPLY>); break;
-  }
-  const int ei = (epi == EPI_GRAM) ? 0 : (epi == EPI_POLY) ? 1 : 2;
-  if (!g_attr_done[ei][dev]) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+  if (!g_attr_done[dev]) {
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(ns_fused_kernel),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
     if (e != cudaSuccess) return e;
-    g_attr_done[ei][dev] = true;
+    g_attr_done[dev] = true;
   }
   if (g_num_sms[dev] == 0) {
     e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
-  const int grid = p.total_tiles < g_num_sms[dev] ? p.total_tiles : g_num_sms[dev];
-  switch (epi) {
-    case EPI_GRAM: ns_gemm_kernel<EPI_GRAM><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
-    case EPI_POLY: ns_gemm_kernel<EPI_POLY><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
-    default: ns_gemm_kernel<EPI_APPLY><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p); break;
-  }
+  const int grid = p.total_tasks < g_num_sms[dev] ? p.total_tasks : g_num_sms[dev];
+  ns_fused_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p);
   return cudaGetLastError();
 }
 
