@@ -77,6 +77,29 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[64];
+
+// A second stream per device and host thread on which the fp32 small-matrix
+// Newton-Schulz runs beside the tensor-core launch (forked from and joined back
+// to the caller's stream with events, so stream order is unchanged).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream t_side[64];
+
+int side_stream(SideStream** out) {
+  int dev = 0;
+  MB_TRY_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MB_ERR_UNSUPPORTED;
+  SideStream& s = t_side[dev];
+  if (!s.stream) {
+    MB_TRY_CUDA(cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking));
+    MB_TRY_CUDA(cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming));
+    MB_TRY_CUDA(cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming));
+  }
+  *out = &s;
+  return MB_OK;
+}
 EncodeTiledFn g_encode = nullptr;
 
 int device_state(DeviceState** out) {
@@ -289,9 +312,18 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     MB_LAUNCH(launch_ns0(p, st), p.total_blocks > 0, MB_MARK_NS0, st);
     return MB_OK;
   }
+  int n_small = 0, n_large = 0;
+  for (int i = 0; i < nb; ++i) (b[i].L.small ? n_small : n_large) += 1;
+  // with tensor-core work to overlap, the fp32 small matrices run on the side stream
+  SideStream* side = nullptr;
+  if (n_small > 0 && n_large > 0) {
+    MB_TRY(side_stream(&side));
+    MB_TRY_CUDA(cudaEventRecord(side->fork, st));
+    MB_TRY_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
+  }
   // small matrices: fp32 SIMT path; one launch for those whose iteration fits in
   // shared memory, one for the rest
-  for (int pass = 0; pass < 2; ++pass) {
+  for (int pass = 0; pass < 2 && n_small > 0; ++pass) {
     const bool in_smem = pass == 0;
     SmallParams sp{};
     sp.steps = steps;
@@ -318,8 +350,14 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     }
     sp.nb = n;
     sp.total_blocks = blocks;
-    MB_LAUNCH(launch_small_ns(sp, in_smem, st), sp.total_blocks > 0, MB_MARK_SMALL_NS, st);
+    if (side) {
+      MB_TRY_CUDA(launch_small_ns(sp, in_smem, side->stream));
+      if (sp.total_blocks > 0) ++g_launch_count;       // no mark: marks time the caller's stream
+    } else {
+      MB_LAUNCH(launch_small_ns(sp, in_smem, st), sp.total_blocks > 0, MB_MARK_SMALL_NS, st);
+    }
   }
+  if (side) MB_TRY_CUDA(cudaEventRecord(side->join, side->stream));
   // large matrices: every step of every bank in one fused tcgen05 launch (up to MAX_NS_BANKS banks each)
   int large[MAX_BANKS], nl = 0;
   for (int i = 0; i < nb; ++i)
@@ -394,6 +432,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     np.next_task = reinterpret_cast<unsigned*>(first.ws + first.L.sync + first.L.sync_bytes - 16);
     MB_LAUNCH(launch_ns_fused(np, st), np.total_tasks > 0, MB_MARK_NS_GEMM, st);
   }
+  if (side) MB_TRY_CUDA(cudaStreamWaitEvent(st, side->join, 0));
   return MB_OK;
 }
 

@@ -299,11 +299,15 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
     if (lane == 0) bulk_wait_read_all();        // the previous chunk's stores have read the buffers
     __syncwarp();
     if (mirror || diag) {
-      const uint32_t lane_off = 2u * (lane & 7);
+      // transposed words: lanes 2r and 2r+1 swap halves so that each lane writes whole 32-bit
+      // words (rows 2r, 2r+1 of one transposed column): the even lane column 2i, the odd lane 2i+1
+      const bool odd = lane & 1;
+      const uint32_t word_off = 4u * ((lane >> 1) & 3);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        *reinterpret_cast<uint16_t*>(bufT + sw64(2 * i, lane >> 3) + lane_off) = static_cast<uint16_t>(pk[i] & 0xFFFFu);
-        *reinterpret_cast<uint16_t*>(bufT + sw64(2 * i + 1, lane >> 3) + lane_off) = static_cast<uint16_t>(pk[i] >> 16);
+        const uint32_t x = __shfl_xor_sync(0xffffffffu, pk[i], 1);
+        const uint32_t w = odd ? ((x >> 16) | (pk[i] & 0xFFFF0000u)) : ((pk[i] & 0xFFFFu) | (x << 16));
+        *reinterpret_cast<uint32_t*>(bufT + sw64(2 * i + (odd ? 1 : 0), lane >> 3) + word_off) = w;
       }
     }
     if (diag) {
@@ -352,7 +356,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
   uint64_t* tempty = tfull + 2;                   // [2] accumulator drained by the epilogue
   uint64_t* slot_full = tempty + 2;               // [TASK_SLOTS] claimed task id written
   uint64_t* slot_empty = slot_full + TASK_SLOTS;  // [TASK_SLOTS] every epilogue warp has read it
-  volatile int* slot = reinterpret_cast<volatile int*>(slot_empty + TASK_SLOTS);
+  uint64_t* tile_done = slot_empty + TASK_SLOTS;  // every epilogue warp's stores of a task are complete
+  volatile int* slot = reinterpret_cast<volatile int*>(tile_done + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(slot + TASK_SLOTS));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -371,6 +376,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       mbar_init(&slot_full[s], 1);
       mbar_init(&slot_empty[s], EPI_WARPS);
     }
+    mbar_init(tile_done, EPI_WARPS);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -409,7 +415,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         const NsBank& B = P.bank[tk.bi];
         int dit, dph;
         if (dependency(tk, dit, dph)) {
-          const unsigned target = static_cast<unsigned>(phase_tiles(B, dph) * EPI_WARPS);
+          const unsigned target = static_cast<unsigned>(phase_tiles(B, dph));
           if (!wait_counter(done_counter(B, tk.mat, dit, dph), target, abort_flag)) {
             fail();
             continue;   // the slot is published; the consumers see the abort and stop
@@ -563,11 +569,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&tempty[buf]);
-        // publish: this warp's part of the tile is in global memory
-        bulk_wait_all();
-        fence_proxy_async_global();
-        __threadfence();
-        red_release_add(done_counter(B, tk.mat, tk.it, tk.ph), 1u);
+        bulk_wait_all();                         // this warp's part of the tile is in global memory
+        mbar_arrive(tile_done);
+      }
+      // one thread publishes the tile once every epilogue warp's stores are complete; it
+      // observes completion k before its own arrival for task k+1, so no phase is skipped
+      if (warp == 2 && lane == 0) {
+        if (mbar_wait_or_abort(tile_done, k & 1, abort_flag)) {
+          fence_proxy_async_global();
+          red_release_add(done_counter(B, tk.mat, tk.it, tk.ph), 1u);
+        } else {
+          fail();
+        }
       }
       __syncwarp();
     }
