@@ -186,22 +186,17 @@ __device__ __forceinline__ bool dependency(const Task& k, int& dit, int& dph) {
 
 // ---------------------------------------------------------------- epilogue
 
-// 32 consecutive bf16 of one row as 16 packed words (zeros outside [0, ncols) or a masked row).
-__device__ __forceinline__ void load_row32_raw(const uint16_t* base, long long ld, int row, int col0, int ncols,
-                                               bool row_ok, uint32_t (&w)[16]) {
-  if (row_ok && col0 + 32 <= ncols) {
+// 16 consecutive bf16 of one row as 8 packed words (zeros outside [0, ncols) or a masked row).
+__device__ __forceinline__ void load_row16_raw(const uint16_t* base, long long ld, int row, int col0, int ncols,
+                                               bool row_ok, uint32_t (&w)[8]) {
+  if (row_ok && col0 + 16 <= ncols) {
     const uint4* p = reinterpret_cast<const uint4*>(base + static_cast<long long>(row) * ld + col0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 v = p[j];
-      w[4 * j + 0] = v.x;
-      w[4 * j + 1] = v.y;
-      w[4 * j + 2] = v.z;
-      w[4 * j + 3] = v.w;
-    }
+    const uint4 v0 = p[0], v1 = p[1];
+    w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+    w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       uint32_t lo = 0, hi = 0;
       if (row_ok && col0 + 2 * i < ncols) lo = base[static_cast<long long>(row) * ld + col0 + 2 * i];
       if (row_ok && col0 + 2 * i + 1 < ncols) hi = base[static_cast<long long>(row) * ld + col0 + 2 * i + 1];
@@ -224,22 +219,33 @@ struct EpiJob {
   const CUtensorMap* st;   // store map of the output
   const uint16_t* ein;     // epilogue input of this matrix (A for POLY, X for APPLY)
   long long ein_ld;
+  // APPLY only: the first step also stores the bf16 residual of X_1 (st_lo), and the
+  // second step adds it back (ein_lo) so that its a*X_1 term uses X_1 to ~16 bits
+  const CUtensorMap* st_lo;
+  const uint16_t* ein_lo;
   int M, N, sym, mat, m0, n0, nt;
   float alpha;
 };
 
+// LO (APPLY only): 0 plain; LO_WRITE also stores the bf16 residual of the output (first
+// step); LO_READ adds the residual stored by the first step to its a*X term (second step).
+constexpr int LO_WRITE = 1, LO_READ = 2;
+
 // Epilogue of one warp: TMEM lanes of quadrant `quad` (tile rows quad*32 + lane),
-// columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`.
+// columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`, taken
+// 16 columns at a time with the next 16 columns' input prefetched.
 // Each 32x32 chunk is staged in the warp's shared buffer and written with a
 // TMA bulk store; a symmetric phase also stores the transposed chunk at the
 // mirrored position.  In a diagonal 128-block the chunks below the diagonal
 // are not stored (their mirror covers them) and the chunk on the diagonal is
 // made symmetric before its store, so every element is written exactly once.
-template <int EPI>
+template <int EPI, int LO>
 __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uint32_t tacc, int quad, int half,
                                          int lane, uint8_t* ebuf) {
+  constexpr bool has_ein = EPI != EPI_GRAM;
+  constexpr bool with_lo = EPI == EPI_APPLY && LO == LO_READ;
   uint8_t* bufD = ebuf;          // [32 rows][32 cols] bf16, 64-byte swizzle
-  uint8_t* bufT = ebuf + 2048;   // [32 cols][32 rows] bf16, 64-byte swizzle
+  uint8_t* bufT = ebuf + 2048;   // [32 cols][32 rows] bf16, 64-byte swizzle (or the residual)
   const int row0 = J.m0 + quad * 32;
   const int row = row0 + lane;
   const bool row_ok = row < J.M;
@@ -247,38 +253,15 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
   const int ncols = J.nt >> 1;
   const int cbeg = half * ncols;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+  const bool odd = lane & 1;
+  const uint32_t word_off = 4u * ((lane >> 1) & 3);
 
-  uint32_t e_cur[16], e_nxt[16];
-  if (EPI != EPI_GRAM) load_row32_raw(J.ein, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, e_cur);
+  uint32_t e_cur[8], e_nxt[8], l_cur[8], l_nxt[8];
+  if (has_ein) load_row16_raw(J.ein, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, e_cur);
+  if (with_lo) load_row16_raw(J.ein_lo, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, l_cur);
 
   for (int c = 0; c < ncols; c += 32) {
     const int col0 = J.n0 + cbeg + c;
-    if (EPI != EPI_GRAM && c + 32 < ncols) load_row32_raw(J.ein, J.ein_ld, row, col0 + 32, J.N, row_ok, e_nxt);
-    uint32_t acc[32];
-    tmem_ld_32x32(tacc + lane_base + static_cast<uint32_t>(cbeg + c), acc);
-    tmem_ld_wait();
-    float o[32];
-    if (EPI == EPI_GRAM) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = J.alpha * __uint_as_float(acc[i]);
-    } else if (EPI == EPI_POLY) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        o[2 * i] = fmaf(P.cc, __uint_as_float(acc[2 * i]), P.cb * bf16_lo(e_cur[i]));
-        o[2 * i + 1] = fmaf(P.cc, __uint_as_float(acc[2 * i + 1]), P.cb * bf16_hi(e_cur[i]));
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        o[2 * i] = J.alpha * fmaf(P.ca, bf16_lo(e_cur[i]), __uint_as_float(acc[2 * i]));
-        o[2 * i + 1] = J.alpha * fmaf(P.ca, bf16_hi(e_cur[i]), __uint_as_float(acc[2 * i + 1]));
-      }
-    }
-    if (EPI != EPI_GRAM) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) e_cur[i] = e_nxt[i];
-    }
-
     // which stores this chunk makes; boxes starting outside the matrix are skipped
     bool direct = row0 < J.M && col0 < J.N, mirror = false, diag = false;
     if (J.sym) {
@@ -292,22 +275,74 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
         else diag = direct;
       }
     }
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+    const bool lo_out = EPI == EPI_APPLY && LO == LO_WRITE && direct;
 
     if (lane == 0) bulk_wait_read_all();        // the previous chunk's stores have read the buffers
     __syncwarp();
-    if (mirror || diag) {
-      // transposed words: lanes 2r and 2r+1 swap halves so that each lane writes whole 32-bit
-      // words (rows 2r, 2r+1 of one transposed column): the even lane column 2i, the odd lane 2i+1
-      const bool odd = lane & 1;
-      const uint32_t word_off = 4u * ((lane >> 1) & 3);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t x = __shfl_xor_sync(0xffffffffu, pk[i], 1);
-        const uint32_t w = odd ? ((x >> 16) | (pk[i] & 0xFFFF0000u)) : ((pk[i] & 0xFFFFu) | (x << 16));
-        *reinterpret_cast<uint32_t*>(bufT + sw64(2 * i + (odd ? 1 : 0), lane >> 3) + word_off) = w;
+    for (int h = 0; h < 2; ++h) {
+      const int hc = col0 + 16 * h;
+      const bool more = c + 16 * h + 16 < ncols;
+      if (has_ein && more) load_row16_raw(J.ein, J.ein_ld, row, hc + 16, J.N, row_ok, e_nxt);
+      if (with_lo && more) load_row16_raw(J.ein_lo, J.ein_ld, row, hc + 16, J.N, row_ok, l_nxt);
+      uint32_t acc[16];
+      tmem_ld_32x16(tacc + lane_base + static_cast<uint32_t>(cbeg + c + 16 * h), acc);
+      tmem_ld_wait();
+      float o[16];
+      if (EPI == EPI_GRAM) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = J.alpha * __uint_as_float(acc[i]);
+      } else if (EPI == EPI_POLY) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[2 * i] = fmaf(P.cc, __uint_as_float(acc[2 * i]), P.cb * bf16_lo(e_cur[i]));
+          o[2 * i + 1] = fmaf(P.cc, __uint_as_float(acc[2 * i + 1]), P.cb * bf16_hi(e_cur[i]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float x0 = bf16_lo(e_cur[i]), x1 = bf16_hi(e_cur[i]);
+          if (with_lo) {
+            x0 += bf16_lo(l_cur[i]);
+            x1 += bf16_hi(l_cur[i]);
+          }
+          o[2 * i] = J.alpha * fmaf(P.ca, x0, __uint_as_float(acc[2 * i]));
+          o[2 * i + 1] = J.alpha * fmaf(P.ca, x1, __uint_as_float(acc[2 * i + 1]));
+        }
+      }
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+      if (direct || diag) {
+        *reinterpret_cast<uint4*>(bufD + sw64(lane, 2 * h)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(bufD + sw64(lane, 2 * h + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+      if (mirror || diag) {
+        // transposed words: lanes 2r and 2r+1 swap halves so that each lane writes whole
+        // 32-bit words (rows 2r, 2r+1 of one transposed column): even lane column 2i, odd 2i+1
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t x = __shfl_xor_sync(0xffffffffu, pk[i], 1);
+          const uint32_t w = odd ? ((x >> 16) | (pk[i] & 0xFFFF0000u)) : ((pk[i] & 0xFFFFu) | (x << 16));
+          *reinterpret_cast<uint32_t*>(bufT + sw64(16 * h + 2 * i + (odd ? 1 : 0), lane >> 3) + word_off) = w;
+        }
+      }
+      if (lo_out) {
+        // residual o - bf16(o), row-major in the (otherwise idle) transposed buffer
+        uint32_t pl[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pl[i] = pack_bf16x2(o[2 * i] - bf16_lo(pk[i]), o[2 * i + 1] - bf16_hi(pk[i]));
+        *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+      }
+      if (has_ein && more) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e_cur[i] = e_nxt[i];
+      }
+      if (with_lo && more) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) l_cur[i] = l_nxt[i];
       }
     }
     if (diag) {
@@ -317,26 +352,25 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 t4 = *reinterpret_cast<const uint4*>(bufT + sw64(lane, j));
+        const uint4 d4 = *reinterpret_cast<const uint4*>(bufD + sw64(lane, j));
         const uint32_t tw[4] = {t4.x, t4.y, t4.z, t4.w};
+        uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int c0 = 8 * j + 2 * q;
-          const uint32_t lo = (c0 < lane) ? (tw[q] & 0xFFFFu) : (pk[4 * j + q] & 0xFFFFu);
-          const uint32_t hi = (c0 + 1 < lane) ? (tw[q] >> 16) : (pk[4 * j + q] >> 16);
-          pk[4 * j + q] = lo | (hi << 16);
+          const uint32_t lo = (c0 < lane) ? (tw[q] & 0xFFFFu) : (dw[q] & 0xFFFFu);
+          const uint32_t hi = (c0 + 1 < lane) ? (tw[q] >> 16) : (dw[q] >> 16);
+          dw[q] = lo | (hi << 16);
         }
+        *reinterpret_cast<uint4*>(bufD + sw64(lane, j)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
       }
-    }
-    if (direct) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(bufD + sw64(lane, j)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && (direct || mirror)) {
       if (direct) tma_store_3d(J.st, bufD, col0, row0, J.mat);
       if (mirror) tma_store_3d(J.st, bufT, row0, col0, J.mat);
+      if (lo_out) tma_store_3d(J.st_lo, bufT, col0, row0, J.mat);
       bulk_commit();
     }
   }
@@ -536,6 +570,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       J.n0 = tk.n0;
       J.nt = tk.nt;
       J.alpha = 1.f;
+      J.st_lo = nullptr;
+      J.ein_lo = nullptr;
       const uint32_t tacc = tmem + buf * ACC_COLS;
       if (tk.ph == EPI_GRAM) {
         if (tk.it == 0) {
@@ -547,23 +583,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         J.ein_ld = 0;
         J.M = J.N = B.m;
         J.sym = 1;
-        epilogue<EPI_GRAM>(P, J, tacc, quad, half, lane, ebuf);
+        epilogue<EPI_GRAM, 0>(P, J, tacc, quad, half, lane, ebuf);
       } else if (tk.ph == EPI_POLY) {
         J.st = &B.st_b;
         J.ein = B.a + tk.mat * B.m_ms;
         J.ein_ld = B.m_ld;
         J.M = J.N = B.m;
         J.sym = 1;
-        epilogue<EPI_POLY>(P, J, tacc, quad, half, lane, ebuf);
+        epilogue<EPI_POLY, 0>(P, J, tacc, quad, half, lane, ebuf);
       } else {
         if (tk.it == 0) J.alpha = B.scale[tk.mat];
         J.st = &B.st_x[iterate_buffer(tk.it + 1)];
         J.ein = B.x[iterate_buffer(tk.it)] + tk.mat * B.x_ms;
         J.ein_ld = B.x_ld;
+        // X_1's residual waits in x[2], which the second APPLY overwrites tile by tile only
+        // after each tile has read its own part
+        if (tk.it == 0 && P.steps > 1) J.st_lo = &B.st_x[2];
+        if (tk.it == 1) J.ein_lo = B.x[2] + tk.mat * B.x_ms;
         J.M = B.tall ? B.n : B.m;
         J.N = B.tall ? B.m : B.n;
         J.sym = 0;
-        epilogue<EPI_APPLY>(P, J, tacc, quad, half, lane, ebuf);
+        if (J.st_lo)
+          epilogue<EPI_APPLY, LO_WRITE>(P, J, tacc, quad, half, lane, ebuf);
+        else if (J.ein_lo)
+          epilogue<EPI_APPLY, LO_READ>(P, J, tacc, quad, half, lane, ebuf);
+        else
+          epilogue<EPI_APPLY, 0>(P, J, tacc, quad, half, lane, ebuf);
       }
       tc_fence_before();
       __syncwarp();

@@ -1,0 +1,154 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+Each workload runs its stated number of consecutive optimizer steps through
+the C ABI (the GPT-2-small and GPT-2-medium sets as one muon_multi_step per
+step, like the benchmark).  On the first and the last step every stage is
+checked against the fp64 oracle fed with the GPU's own intermediates:
+momentum and the update on every element (the GPT-2-medium banks on sampled
+matrices), Newton-Schulz and NorMuon on sampled matrices of every bank.
+
+The low-rank gradients of the multi-bank workloads cycle through the first
+two seeded draws (as the benchmark does), which keeps the host-side input
+generation of twenty GPT-2-medium steps within seconds.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from gpu_util import (MOMENTUM_TOL, STATE_TOL, UPDATE_TOL, check_ns, check_update, f32, ns_tol, to_dev, u16,
+                      u_bound, ws_matrix)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nss():
+    from newton_schulz_stacked_gb300.build import build_library
+    build_library()
+    import newton_schulz_stacked_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    m.load_library()
+    return m
+
+
+def _sample(batch, n, seed):
+    if batch <= n:
+        return list(range(batch))
+    rng = np.random.default_rng(seed)
+    return sorted(set([0, batch - 1] + rng.choice(batch, size=n - 2, replace=False).tolist()))
+
+
+class Run:
+    """A workload's banks on the GPU, stepped through muon_multi_step (or muon_bank_step)."""
+
+    def __init__(self, nss, wid, cycle_grads=None):
+        self.nss, self.wl, self.wid = nss, synth.WORKLOADS[wid], wid
+        self.cycle = cycle_grads
+        self.banks, self.grad_cache = [], {}
+        for bi in range(len(self.wl.banks)):
+            w, mant, mom, row = synth.init_state(wid, bi)
+            self.banks.append(nss.BankState(to_dev(w), None, to_dev(mom), to_dev(mant),
+                                            to_dev(row) if self.wl.normuon else None))
+        self.ws = None
+
+    def grads(self, step):
+        key = ((step - 1) % self.cycle) + 1 if self.cycle else step
+        if key not in self.grad_cache:
+            self.grad_cache[key] = [synth.grad(self.wid, key, bi) for bi in range(len(self.wl.banks))]
+        return self.grad_cache[key]
+
+    def step(self, step):
+        g = self.grads(step)
+        for b, gb in zip(self.banks, g):
+            b.grad = to_dev(gb)
+        if self.ws is None:
+            self.ws = torch.empty(self.nss.mb_multi_workspace_bytes(self.banks, self.wl.normuon), dtype=torch.uint8,
+                                  device="cuda:0")
+        self.nss.muon_multi_step(self.banks, self.wl.lr, self.wl.wd, self.wl.mu, normuon=self.wl.normuon,
+                                 beta2=self.wl.beta2, ns_steps=self.wl.ns_steps, workspace=self.ws)
+        torch.cuda.synchronize()
+        assert self.nss.mb_sync_status() == 0
+        return g
+
+    def snapshot(self):
+        return [(u16(b.bank), u16(b.mantissa), f32(b.momentum), f32(b.row_state) if b.row_state is not None else None)
+                for b in self.banks]
+
+    def views(self, bi):
+        """u and v of bank bi inside the multi-bank workspace (banks are laid out one after another)."""
+        off = 0
+        for j, spec in enumerate(self.wl.banks):
+            shape = spec.shape
+            u_off, v_off, pitch = self.nss.mb_workspace_views(shape, self.wl.normuon, self.wl.ns_steps)
+            if j == bi:
+                return ws_matrix(self.ws, off + u_off, shape, pitch), ws_matrix(self.ws, off + v_off, shape, pitch)
+            off += self.nss.mb_workspace_bytes(shape, self.wl.normuon)
+        raise IndexError(bi)
+
+
+def _check_step(run, before, grads, ns_sample=6, elementwise_all=True):
+    wl = run.wl
+    for bi, spec in enumerate(wl.banks):
+        B, R, C = spec.shape
+        w0, m0, b0, s0 = before[bi]
+        g = grads[bi]
+        bank = run.banks[bi]
+        u_gpu, v_gpu = run.views(bi)
+        mats = list(range(B)) if elementwise_all else _sample(B, ns_sample, 7 + bi)
+        b_gpu = f32(bank.momentum)
+        for k in mats:
+            b_ref, _, u_exact = O.momentum(g[k], b0[k], wl.mu)
+            assert O.rel_frobenius(b_gpu[k], b_ref) <= MOMENTUM_TOL, (spec.name, k)
+            assert np.all(np.abs(O.bf16_bits_to_f64(u_gpu[k]) - u_exact) <= u_bound(u_exact, g[k], b_ref)), (spec.name, k)
+        ns_mats = _sample(B, ns_sample, 11 + bi)
+        errs = check_ns(u_gpu, v_gpu, wl.ns_steps, ns_mats)
+        assert errs.max() <= ns_tol(R, C), (spec.name, errs)
+        for k in spec.dead_slots:
+            assert not np.any(v_gpu[k]) and not np.any(u16(bank.bank)[k]), (spec.name, k)
+        w1, m1 = u16(bank.bank), u16(bank.mantissa)
+        if wl.normuon:
+            state = f32(bank.row_state)
+            vhat = []
+            for k in mats:
+                vh, s = O.normuon(O.bf16_bits_to_f64(v_gpu[k]), s0[k], wl.beta2)
+                assert O.rel_frobenius(state[k], s) <= STATE_TOL, (spec.name, k)
+                vhat.append(vh)
+            assert check_update(w0, m0, v_gpu, w1, m1, wl.lr, wl.wd, R, C, mats=mats, vhat=vhat) <= UPDATE_TOL
+        else:
+            assert check_update(w0, m0, v_gpu, w1, m1, wl.lr, wl.wd, R, C, mats=mats) <= UPDATE_TOL
+
+
+def _run_and_check(nss, wid, cycle=None, ns_sample=6, elementwise_all=True):
+    run = Run(nss, wid, cycle)
+    last = run.wl.steps
+    for step in range(1, last + 1):
+        if step in (1, last):
+            before = run.snapshot()
+            grads = run.step(step)
+            _check_step(run, before, grads, ns_sample, elementwise_all)
+        else:
+            run.step(step)
+    return run
+
+
+def test_tiny_bank(nss):
+    _run_and_check(nss, 1)
+
+
+def test_gpt2_small_attention_bank(nss):
+    _run_and_check(nss, 2)
+
+
+def test_gpt2_small_mlp_bank_with_dead_slot(nss):
+    _run_and_check(nss, 3)
+
+
+def test_gpt2_small_full_step(nss):
+    """The benchmark's workload: attention + MLP banks and both gates in one launch sequence."""
+    _run_and_check(nss, 4, cycle=2, ns_sample=6)
+
+
+def test_gpt2_medium_normuon(nss):
+    _run_and_check(nss, 5, cycle=2, ns_sample=4, elementwise_all=False)
