@@ -102,6 +102,25 @@ def profiled_traffic(workload):
     return d.get("workloads", {}).get(str(workload), {}).get("bytes_per_launch")
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (x itself outside torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = device if device is not None and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, steps: int, slowest_ms: float) -> float:
+    """Whole-job rate: every rank runs `steps` steps; the job lasts as long as its slowest rank."""
+    return world * steps / (slowest_ms / 1e3)
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -298,16 +317,12 @@ def run_native(args):
         if world > 1:
             dist.barrier()
     launches = nss.mb_launch_count() - n0
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
     if nss.mb_sync_status() != 0:
         raise RuntimeError("device-side status set during the timed steps")
 
     ms_per_step = elapsed_ms / args.steps
-    value = world * args.steps / (elapsed_ms / 1e3)
+    value = job_rate(world, args.steps, elapsed_ms)
 
     # per-stage device time from the library's stage events (same stream, same timed steps)
     tot = timer.totals()
@@ -408,12 +423,8 @@ def run_native(args):
         e2e_run(k_e2e)
         e1.record(main_s)
         torch.cuda.synchronize()
-        e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * k_e2e / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3), dev)
+        e2e = {"value": job_rate(world, k_e2e, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k_e2e,
                "what": "pinned host gradients -> device, muon_multi_step, updated bf16 weights -> pinned host; "
                        "copies on two copy streams overlap the neighbouring steps' compute"}
