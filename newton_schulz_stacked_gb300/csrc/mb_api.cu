@@ -176,7 +176,8 @@ Layout make_layout(const mb_shape& s, int normuon, size_t base) {
   L.m = L.tall ? s.cols : s.rows;
   L.n = L.tall ? s.rows : s.cols;
   L.small = L.m <= SMALL_M;
-  L.ld = static_cast<int>(align_up(static_cast<size_t>(s.cols), 8));
+  // large banks: a multiple of 64 columns, so that an MN-major operand box of 64-column chunks stays in its row
+  L.ld = static_cast<int>(align_up(static_cast<size_t>(s.cols), L.small ? 8 : 64));
   L.ldm = static_cast<int>(align_up(static_cast<size_t>(L.m), 8));
   const size_t E = static_cast<size_t>(s.rows) * s.cols;
   L.P = static_cast<int>((E + EW_CHUNK - 1) / EW_CHUNK);
@@ -241,6 +242,26 @@ int encode_map(CUtensorMap* map, const void* base, int inner, int rows, int batc
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     g_last_cuda_error = "cuTensorMapEncodeTiled failed (" + std::to_string(static_cast<int>(r)) + ")";
+    return MB_ERR_CUDA;
+  }
+  return MB_OK;
+}
+
+// MN-major view of a bf16 buffer of `batch` matrices of `rows` x `ld` (ld a multiple of 64):
+// {64 columns, rows, ld / 64 chunks, matrix}; one box is 64 rows of `chunks` 64-column chunks,
+// landing chunk after chunk (8 KB each) in the 128-byte swizzle.
+int encode_mn_map(CUtensorMap* map, const void* base, int rows, int batch, int ld, int chunks) {
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(ld / 64),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld) * 2, 128,
+                                 static_cast<cuuint64_t>(ld) * static_cast<cuuint64_t>(rows) * 2};
+  const cuuint32_t box[4] = {64, 64, static_cast<cuuint32_t>(chunks), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled (4-D) failed (" + std::to_string(static_cast<int>(r)) + ")";
     return MB_ERR_CUDA;
   }
   return MB_OK;
@@ -384,16 +405,21 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
       NsBank& nb_ = np.bank[j];
       for (int t = 0; t < 3; ++t) {
         MB_TRY(encode_map(&nb_.xk[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 128));
-        MB_TRY(encode_map(&nb_.xmn[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 64));
+        MB_TRY(encode_map(&nb_.xk2[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 256));
+        MB_TRY(encode_mn_map(&nb_.xmn2[t], k.ws + L.x[t], L.rows, L.batch, L.ld, 2));
+        MB_TRY(encode_mn_map(&nb_.xmn4[t], k.ws + L.x[t], L.rows, L.batch, L.ld, 4));
         MB_TRY(encode_map(&nb_.st_x[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 32, 32,
                           CU_TENSOR_MAP_SWIZZLE_64B));
         nb_.x[t] = k.at<uint16_t>(L.x[t]);
       }
       MB_TRY(encode_map(&nb_.ak, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 128));
+      MB_TRY(encode_map(&nb_.ak2, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 256));
       MB_TRY(encode_map(&nb_.bk, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 128));
+      MB_TRY(encode_map(&nb_.bk2, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 256));
       MB_TRY(encode_map(&nb_.st_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       MB_TRY(encode_map(&nb_.st_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       nb_.a = k.at<uint16_t>(L.a);
+      nb_.b = k.at<uint16_t>(L.b);
       nb_.x_ld = L.ld;
       nb_.x_ms = static_cast<long long>(L.rows) * L.ld;
       nb_.m_ld = L.ldm;

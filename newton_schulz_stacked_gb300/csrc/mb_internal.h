@@ -93,13 +93,18 @@ constexpr int MAX_NS_STEPS = 16;
 
 // One large bank in the fused Newton-Schulz launch.  x[0] holds u; the
 // iterates X_1, X_2, ... alternate between x[1] and x[2].
+// Every operand tile of one 64-deep k-block is a single TMA box: K-major boxes
+// of 128 or 256 rows, and MN-major boxes of 2 or 4 chunks of 64 columns through
+// a 4-D view {64 columns, rows, row pitch / 64 chunks, matrix} of an X buffer
+// (large banks pitch their X buffers to a multiple of 64 columns for it).
 struct NsBank {
-  CUtensorMap xk[3];                // X buffers as K-major 128x64 operand tiles
-  CUtensorMap xmn[3];               // the same buffers as MN-major 64x64 operand tiles
-  CUtensorMap ak, bk;               // A and B as K-major operand tiles
+  CUtensorMap xk[3], xk2[3];        // X buffers, K-major boxes of 128 and 256 rows x 64
+  CUtensorMap xmn2[3], xmn4[3];     // X buffers, MN-major boxes of 64 K rows x 128 and 256 columns
+  CUtensorMap ak, ak2, bk, bk2;     // A and B, K-major boxes of 128 and 256 rows x 64
   CUtensorMap st_x[3], st_a, st_b;  // 32x32 store boxes (64-byte swizzle)
-  const uint16_t* x[3];
-  const uint16_t* a;
+  uint16_t* x[3];                   // X buffers (epilogue inputs and direct stores)
+  uint16_t* a;                      // A and B (direct stores; A is POLY's epilogue input)
+  uint16_t* b;
   long long x_ld, x_ms, m_ld, m_ms;  // pitches (elements) and matrix strides
   const float* scale;               // per-matrix 1/(||u||_F + eps)
   unsigned* done;                   // completion counters [batch][MAX_NS_STEPS][3], zeroed before launch

@@ -24,9 +24,15 @@
 // earlier tasks and all CTAs are resident, so the earliest unfinished task
 // can always run; each wait is bounded all the same.
 //
-// CTA roles (10 warps):
-//   warp 0 lane 0 : claims tasks, waits for their inputs, TMA producer of a
-//                   STAGES-deep ring of (A 128x64, B 256x64) bf16 tiles
+// CTA roles (11 warps):
+//   warp 10 lane 0: scheduler: claims the next task, decodes it and waits until
+//                   its inputs are stored, one task ahead of the producer, and
+//                   hands the decoded task to the other roles through a ring of
+//                   task records in shared memory
+//   warp 0 lane 0 : TMA producer of a STAGES-deep ring of (A 128x64, B 256x64)
+//                   bf16 tiles, one TMA box per operand and k-block (a producer
+//                   thread pays about as much per TMA instruction as an MMA of
+//                   one 16-deep slice takes, so each operand is a single box)
 //   warp 1        : owns 512 TMEM columns = two 256-column fp32 accumulators;
 //                   lane 0 issues tcgen05.mma (K = 16 per instruction)
 //   warps 2..9    : epilogue, two warps per 32-lane TMEM quadrant (each takes
@@ -50,13 +56,16 @@ constexpr int EPI_BUF_BYTES = 4096;          // per epilogue warp: 32x32 bf16 ch
 constexpr int EPI_SMEM = EPI_WARPS * EPI_BUF_BYTES;
 constexpr int TASK_SLOTS = 4;                // claimed tasks in flight inside a CTA
 constexpr int GEMM_SMEM = TILE_SMEM + EPI_SMEM + 1024 /* alignment slack */ + 512 /* barriers, slots */;
-constexpr int GEMM_THREADS = 32 * (2 + EPI_WARPS);
+constexpr int SCHED_WARP = 2 + EPI_WARPS;
+constexpr int GEMM_THREADS = 32 * (3 + EPI_WARPS);
 constexpr uint32_t ACC_COLS = 256;          // one accumulator
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
 // ---------------------------------------------------------------- tasks
 
+// One task, as the scheduler hands it over (t < 0: no more tasks).
 struct Task {
+  int t;                 // task index
   int it, ph, bi, mat;   // step, phase, bank, matrix
   int m0, n0, nt;        // output tile origin and width (128 or 256)
 };
@@ -64,6 +73,7 @@ struct Task {
 __device__ __forceinline__ int iterate_buffer(int k) { return k == 0 ? 0 : 1 + ((k - 1) & 1); }
 
 __device__ __forceinline__ void decode_task(const NsParams& P, int t, Task& k) {
+  k.t = t;
   k.it = t / P.tasks_per_iter;
   int r = t - k.it * P.tasks_per_iter;
   k.ph = (r >= P.phase_begin[EPI_APPLY]) ? EPI_APPLY : (r >= P.phase_begin[EPI_POLY]) ? EPI_POLY : EPI_GRAM;
@@ -108,7 +118,8 @@ __device__ __forceinline__ unsigned* done_counter(const NsBank& B, int mat, int 
   return B.done + (static_cast<size_t>(mat) * MAX_NS_STEPS + it) * 3 + ph;
 }
 
-// Operands of a task's GEMM.
+// Operands of a task's GEMM: the map of each operand's single box per k-block
+// (A: 128 rows or 128 MN columns; B: nt rows or nt MN columns).
 struct Operands {
   const CUtensorMap* a;
   const CUtensorMap* b;
@@ -117,24 +128,32 @@ struct Operands {
 
 __device__ __forceinline__ Operands task_operands(const NsBank& B, const Task& k) {
   const int cur = iterate_buffer(k.it);
+  const bool wide = k.nt > 128;
   Operands o;
   if (k.ph == EPI_GRAM) {
-    o.a = o.b = B.tall ? &B.xmn[cur] : &B.xk[cur];
+    if (B.tall) {        // A = X^T X: columns of X on both sides
+      o.a = &B.xmn2[cur];
+      o.b = wide ? &B.xmn4[cur] : &B.xmn2[cur];
+    } else {             // A = X X^T: rows of X on both sides
+      o.a = &B.xk[cur];
+      o.b = wide ? &B.xk2[cur] : &B.xk[cur];
+    }
     o.a_mn = o.b_mn = B.tall;
     o.K = B.n;
   } else if (k.ph == EPI_POLY) {
-    o.a = o.b = &B.ak;
+    o.a = &B.ak;
+    o.b = wide ? &B.ak2 : &B.ak;
     o.a_mn = o.b_mn = 0;
     o.K = B.m;
   } else {
     if (!B.tall) {       // X' = a X + B X: rows of B (K-major), X as MN-major tiles
       o.a = &B.bk;
-      o.b = &B.xmn[cur];
+      o.b = wide ? &B.xmn4[cur] : &B.xmn2[cur];
       o.a_mn = 0;
       o.b_mn = 1;
     } else {             // X' = a X + X B: rows of X and of B, both K-major
       o.a = &B.xk[cur];
-      o.b = &B.bk;
+      o.b = wide ? &B.bk2 : &B.bk;
       o.a_mn = 0;
       o.b_mn = 0;
     }
@@ -388,11 +407,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;               // [2] accumulator ready for the epilogue
   uint64_t* tempty = tfull + 2;                   // [2] accumulator drained by the epilogue
-  uint64_t* slot_full = tempty + 2;               // [TASK_SLOTS] claimed task id written
-  uint64_t* slot_empty = slot_full + TASK_SLOTS;  // [TASK_SLOTS] every epilogue warp has read it
-  uint64_t* tile_done = slot_empty + TASK_SLOTS;  // every epilogue warp's stores of a task are complete
-  volatile int* slot = reinterpret_cast<volatile int*>(tile_done + 1);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(slot + TASK_SLOTS));
+  uint64_t* slot_full = tempty + 2;               // [TASK_SLOTS] task record written
+  uint64_t* slot_empty = slot_full + TASK_SLOTS;  // [TASK_SLOTS] producer, MMA and epilogue warps have read it
+  uint64_t* prod_took = slot_empty + TASK_SLOTS;  // [TASK_SLOTS] the producer has started the task
+  uint64_t* tile_done = prod_took + TASK_SLOTS;   // every epilogue warp's stores of a task are complete
+  Task* rec = reinterpret_cast<Task*>(tile_done + 2);   // [TASK_SLOTS] (16-byte aligned)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rec + TASK_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -408,7 +428,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
     }
     for (int s = 0; s < TASK_SLOTS; ++s) {
       mbar_init(&slot_full[s], 1);
-      mbar_init(&slot_empty[s], EPI_WARPS);
+      mbar_init(&slot_empty[s], EPI_WARPS + 2);
+      mbar_init(&prod_took[s], 1);
     }
     mbar_init(tile_done, EPI_WARPS);
     *abort_flag = 0;
@@ -428,62 +449,92 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
     *abort_flag = 1;
   };
 
-  if (warp == 0) {
+  if (warp == SCHED_WARP) {
     if (lane == 0) {
-      // ---------------- task claims + TMA producer
+      // ---------------- scheduler: claim, decode, wait for the inputs; at most one task ahead of the producer
+      for (uint32_t k = 0;; ++k) {
+        const int s = k % TASK_SLOTS;
+        if (k >= TASK_SLOTS && !mbar_wait_or_abort(&slot_empty[s], ((k / TASK_SLOTS) - 1) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        if (k >= 1) {
+          const uint32_t p = k - 1;
+          if (!mbar_wait_or_abort(&prod_took[p % TASK_SLOTS], (p / TASK_SLOTS) & 1, abort_flag)) {
+            fail();
+            break;
+          }
+        }
+        int t = *abort_flag ? -1 : static_cast<int>(atomicAdd(P.next_task, 1u));
+        if (t >= P.total_tasks) t = -1;
+        Task tk;
+        tk.t = -1;
+        if (t >= 0) {
+          decode_task(P, t, tk);
+          int dit, dph;
+          if (dependency(tk, dit, dph)) {
+            const NsBank& B = P.bank[tk.bi];
+            const unsigned target = static_cast<unsigned>(phase_tiles(B, dph));
+            if (!wait_counter(done_counter(B, tk.mat, dit, dph), target, abort_flag)) {
+              fail();
+              break;   // the consumers see the abort and stop
+            }
+          }
+        }
+        rec[s] = tk;
+        mbar_arrive(&slot_full[s]);
+        if (tk.t < 0) break;
+      }
+    }
+  } else if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
       for (int b = 0; b < P.nbank; ++b) {
         tma_prefetch_map(&P.bank[b].ak);
+        tma_prefetch_map(&P.bank[b].ak2);
         tma_prefetch_map(&P.bank[b].bk);
+        tma_prefetch_map(&P.bank[b].bk2);
       }
+      int st = 0;
+      uint32_t ph = 0;
       uint32_t it = 0;
       for (uint32_t k = 0;; ++k) {
         const int s = k % TASK_SLOTS;
-        if (k >= TASK_SLOTS && !mbar_wait_or_abort(&slot_empty[s], ((k / TASK_SLOTS) - 1) & 1, abort_flag)) fail();
-        int t = *abort_flag ? -1 : static_cast<int>(atomicAdd(P.next_task, 1u));
-        if (t >= P.total_tasks) t = -1;
-        slot[s] = t;
-        mbar_arrive(&slot_full[s]);
-        if (t < 0) break;
-        Task tk;
-        decode_task(P, t, tk);
-        const NsBank& B = P.bank[tk.bi];
-        int dit, dph;
-        if (dependency(tk, dit, dph)) {
-          const unsigned target = static_cast<unsigned>(phase_tiles(B, dph));
-          if (!wait_counter(done_counter(B, tk.mat, dit, dph), target, abort_flag)) {
-            fail();
-            continue;   // the slot is published; the consumers see the abort and stop
-          }
-          fence_proxy_async_global();
+        if (!mbar_wait_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
+          fail();
+          break;
         }
-        const Operands op = task_operands(B, tk);
+        const Task tk = rec[s];
+        mbar_arrive(&prod_took[s]);
+        mbar_arrive(&slot_empty[s]);
+        if (tk.t < 0 || *abort_flag) break;
+        // the scheduler acquired the inputs of this task; order them before this thread's TMA reads
+        fence_proxy_async_global();
+        const Operands op = task_operands(P.bank[tk.bi], tk);
         const int KB = (op.K + BK - 1) / BK;
         const uint32_t bytes = A_TILE_BYTES + tk.nt * BK * 2;
+        const int ma = tk.m0 >> 6, nb = tk.n0 >> 6;
+        bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int st = it % STAGES;
-          const uint32_t use = it / STAGES;
-          if (use > 0 && !mbar_wait_or_abort(&empty[st], (use - 1) & 1, abort_flag)) {
+          if (it >= STAGES && !mbar_wait_or_abort(&empty[st], ph ^ 1u, abort_flag)) {
             fail();
+            ok = false;
             break;
           }
           mbar_expect_tx(&full[st], bytes);
           uint8_t* a = sA + st * A_TILE_BYTES;
           uint8_t* b = sB + st * B_TILE_BYTES;
           const int k0 = kb * BK;
-          if (!op.a_mn) {
-            tma_load_3d(a, op.a, &full[st], k0, tk.m0, tk.mat);
-          } else {
-            tma_load_3d(a, op.a, &full[st], tk.m0, k0, tk.mat);
-            tma_load_3d(a + 8192, op.a, &full[st], tk.m0 + 64, k0, tk.mat);
-          }
-          if (!op.b_mn) {
-            for (int h = 0; h < tk.nt / 128; ++h)
-              tma_load_3d(b + h * 16384, op.b, &full[st], k0, tk.n0 + 128 * h, tk.mat);
-          } else {
-            for (int h = 0; h < tk.nt / 64; ++h)
-              tma_load_3d(b + h * 8192, op.b, &full[st], tk.n0 + 64 * h, k0, tk.mat);
+          if (!op.a_mn) tma_load_3d(a, op.a, &full[st], k0, tk.m0, tk.mat);
+          else tma_load_4d(a, op.a, &full[st], 0, k0, ma, tk.mat);
+          if (!op.b_mn) tma_load_3d(b, op.b, &full[st], k0, tk.n0, tk.mat);
+          else tma_load_4d(b, op.b, &full[st], 0, k0, nb, tk.mat);
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1u;
           }
         }
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
@@ -496,10 +547,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
           fail();
           break;
         }
-        const int t = slot[s];
-        if (t < 0 || *abort_flag) break;
-        Task tk;
-        decode_task(P, t, tk);
+        const Task tk = rec[s];
+        mbar_arrive(&slot_empty[s]);
+        if (tk.t < 0 || *abort_flag) break;
         const Operands op = task_operands(P.bank[tk.bi], tk);
         const int KB = (op.K + BK - 1) / BK;
         const uint32_t buf = k & 1;
@@ -545,12 +595,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         fail();
         break;
       }
-      const int t = slot[s];
+      const Task tk = rec[s];
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_empty[s]);
-      if (t < 0) break;
-      Task tk;
-      decode_task(P, t, tk);
+      if (tk.t < 0) break;
       const NsBank& B = P.bank[tk.bi];
       const uint32_t buf = k & 1;
       if (!mbar_wait_or_abort(&tfull[buf], (k >> 1) & 1, abort_flag)) {
