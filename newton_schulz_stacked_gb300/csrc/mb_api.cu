@@ -443,15 +443,17 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     }
     // task numbering inside one step: phase, then bank, then matrix and tile
     int per_iter = 0;
+    np.nseg = 0;
     for (int ph = EPI_GRAM; ph <= EPI_APPLY; ++ph) {
-      np.phase_begin[ph] = per_iter;
-      int in_phase = 0;
       for (int j = 0; j < gn; ++j) {
-        np.bank[j].begin[ph] = in_phase;
-        in_phase += np.bank[j].batch * (ph == EPI_APPLY ? np.bank[j].apply_tiles : np.bank[j].sym_tiles);
+        np.seg_begin[np.nseg] = per_iter;
+        np.seg_bank[np.nseg] = static_cast<unsigned char>(j);
+        np.seg_ph[np.nseg] = static_cast<unsigned char>(ph);
+        ++np.nseg;
+        per_iter += np.bank[j].batch * (ph == EPI_APPLY ? np.bank[j].apply_tiles : np.bank[j].sym_tiles);
       }
-      per_iter += in_phase;
     }
+    np.seg_begin[np.nseg] = per_iter;
     np.tasks_per_iter = per_iter;
     np.total_tasks = per_iter * steps;
     const Bank& first = b[large[g0]];

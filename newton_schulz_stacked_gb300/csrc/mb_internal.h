@@ -111,13 +111,15 @@ struct NsBank {
   int batch, rows, cols, m, n, tall;
   int T, sym_tiles;                 // 128-blocks per side of A; tiles per matrix of GRAM and POLY
   int tn, apply_tiles;              // 256-wide column tiles and tiles per matrix of APPLY
-  int begin[3];                     // first task of this bank within each phase of one iteration
 };
 
 struct NsParams {
   NsBank bank[MAX_NS_BANKS];
   int nbank, steps;
-  int phase_begin[3];               // first task of each phase within one iteration
+  // one step's tasks come as (bank, phase) segments in this order; seg_begin[nseg] is the step's size
+  int nseg;
+  int seg_begin[3 * MAX_NS_BANKS + 1];
+  unsigned char seg_bank[3 * MAX_NS_BANKS], seg_ph[3 * MAX_NS_BANKS];
   int tasks_per_iter, total_tasks;
   unsigned* next_task;              // dynamic scheduler, zeroed before launch
   float ca, cb, cc;

@@ -15,8 +15,9 @@
 // block twice, directly and mirrored, so the next phase reads a full matrix.
 //
 // Scheduling.  The work of all steps is one list of tasks (an output tile of
-// one phase of one matrix), ordered by step, then phase, then bank, matrix
-// and tile.  Persistent CTAs, one per SM, claim tasks in that order from a
+// one phase of one matrix), ordered by step, then by (bank, phase) segment in
+// the order the host gives (any order that puts each bank's GRAM before its
+// POLY before its APPLY), then matrix and tile.  Persistent CTAs, one per SM, claim tasks in that order from a
 // global counter.  A task's producer first waits until every tile of the
 // previous phase of the same matrix has been stored (per-matrix completion
 // counters, release/acquire at GPU scope), so phases overlap across matrices
@@ -76,13 +77,12 @@ __device__ __forceinline__ void decode_task(const NsParams& P, int t, Task& k) {
   k.t = t;
   k.it = t / P.tasks_per_iter;
   int r = t - k.it * P.tasks_per_iter;
-  k.ph = (r >= P.phase_begin[EPI_APPLY]) ? EPI_APPLY : (r >= P.phase_begin[EPI_POLY]) ? EPI_POLY : EPI_GRAM;
-  r -= P.phase_begin[k.ph];
-  int bi = 0;
-  while (bi + 1 < P.nbank && r >= P.bank[bi + 1].begin[k.ph]) ++bi;
-  k.bi = bi;
-  const NsBank& B = P.bank[bi];
-  r -= B.begin[k.ph];
+  int g = 0;
+  while (g + 1 < P.nseg && r >= P.seg_begin[g + 1]) ++g;
+  k.bi = P.seg_bank[g];
+  k.ph = P.seg_ph[g];
+  r -= P.seg_begin[g];
+  const NsBank& B = P.bank[k.bi];
   k.m0 = k.n0 = 0;
   k.nt = 128;
   if (k.ph != EPI_APPLY) {
