@@ -8,7 +8,7 @@ attn_gate (10, 6, 12): momentum, Frobenius normalisation, five quintic
 Newton-Schulz iterations and the bf16 + mantissa update, all in this
 repository's CUDA kernels.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--workload 4|5]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--workload 4|5|6]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 of the workload (the step has no cross-GPU exchange on one node's banks);
@@ -41,7 +41,7 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--workload", type=int, default=4, choices=[4, 5])
+    p.add_argument("--workload", type=int, default=4, choices=[4, 5, 6])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -353,8 +353,9 @@ def run_native(args):
 
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # two full steps of every bank (workload 4: ~11 s on 16 cores), or a slice of the larger one
-        sample = {spec.name: spec.batch for spec in wl.banks} if args.workload == 4 else {"attn": 8, "mlp": 4}
+        # two full steps of every bank (workload 4: ~11 s on 16 cores), or a slice of the larger ones
+        sample = ({spec.name: spec.batch for spec in wl.banks} if args.workload == 4
+                  else {"attn": 8, "mlp": 4, "qk": 16, "vo": 8})
         t0 = time.perf_counter()
         ests = [cpu_oracle_sample(wl, sample, seed_step=k + 1) for k in range(2)]
         est = statistics.mean(e[0] for e in ests)

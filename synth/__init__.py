@@ -15,6 +15,13 @@ Workloads follow the speedrun pages' parameter banks:
   * Gate parameters smear_gate (1, 12, 768) and attn_gate (10, 6, 12).
   * GPT-2-medium banks (96, 1024, 1024) and (48, 4096, 1024) (Track-2
     record 7, model dim 1024).
+  * The successor banks of the same write-up's section 1.1: qk_bank
+    (slots, 2*head_dim, model_dim), vo_bank (slots, hdim, model_dim) and
+    mlp_bank (12, 2, 2816, 768) viewed as (24, 2816, 768), whose slot 7 of
+    the (12, 2) view stays dead.  Slot counts are not printed; the reading
+    here is 10 layers x 6 heads of 128 = 60 qk slots padded to 64, and
+    10 layers x (v, o) = 20 vo slots of 768 x 768 padded to 24, the padding
+    slots dead.
 
 Seeds: initial state of bank b in workload w uses PCG64(1000*w + b); the
 gradient of optimizer step k >= 1 uses PCG64(1000*w + 10*k + b).
@@ -78,6 +85,11 @@ WORKLOADS = {
         BankSpec("attn", 96, 1024, 1024, "lowrank"),
         BankSpec("mlp", 48, 4096, 1024, "lowrank"),
     ), steps=20, normuon=True),
+    6: Workload(6, "successor banks qk 64x256x768 + vo 24x768x768 + mlp 24x2816x768", (
+        BankSpec("qk", 64, 256, 768, "lowrank", dead_slots=(60, 61, 62, 63)),
+        BankSpec("vo", 24, 768, 768, "lowrank", dead_slots=(20, 21, 22, 23)),
+        BankSpec("mlp", 24, 2816, 768, "lowrank", dead_slots=(14, 15)),
+    ), steps=3),
 }
 
 

@@ -152,3 +152,9 @@ def test_gpt2_small_full_step(nss):
 
 def test_gpt2_medium_normuon(nss):
     _run_and_check(nss, 5, cycle=2, ns_sample=4, elementwise_all=False)
+
+
+def test_successor_banks(nss):
+    """qk_bank 64x256x768 (wide: A is 256 x 256), vo_bank 24x768x768 and the 2816-wide MLP bank,
+    with their padding and dead slots, in one launch sequence."""
+    _run_and_check(nss, 6, cycle=2, ns_sample=5)
