@@ -51,8 +51,17 @@ def ws_matrix(ws: torch.Tensor, offset: int, shape, pitch: int) -> np.ndarray:
     return host.view(np.uint16).reshape(B, R, pitch)[:, :, :C].copy()
 
 
-def ns_tol(rows, cols):
-    return NS_SMALL_TOL if min(rows, cols) <= 64 else NS_TOL
+def ns_tol(rows, cols, steps=5):
+    """relF bound of the GPU Newton-Schulz output against the fp64 iteration.
+
+    The bound is stated for the method's 5 steps.  Each bf16-rounded step adds
+    error (a bf16 emulation of the kernel's rounding gives about 1.0e-2 at 5
+    steps, 1.9e-2 at 8, 3.4e-2 at 16 on Gaussian 256x384), so beyond 5 steps
+    the bound grows by the same 4e-3 per step that gives 2e-2 at 5.
+    """
+    if min(rows, cols) <= 64:
+        return NS_SMALL_TOL
+    return NS_TOL if steps <= 5 else NS_TOL * steps / 5
 
 
 def check_ns(u_bits, v_bits, steps=5, mats=None):
