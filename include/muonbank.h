@@ -124,6 +124,22 @@ int muon_multi_step(const mb_bank_desc* banks, int n_banks, float lr, float wd, 
                     int normuon, float beta2, int ns_steps, void* workspace,
                     size_t workspace_bytes, void* cuda_stream);
 
+/* muon_multi_step with each bank's hyperparameters read from device memory when
+ * the step runs, so that a captured CUDA graph of the step can be replayed with
+ * new values ("Unified zero-copy optimizer" write-up, section 4: all banks' step
+ * scalars in one fp32 device buffer, uploaded once per step, read by the graph).
+ *   scalars_dev : device pointer, 16-byte aligned, n_banks x {lr, wd, mu, beta2}
+ *                 fp32 (beta2 only read with normuon); the caller owns it and may
+ *                 rewrite it between steps (stream-ordered with the step).
+ * Results are bit-identical to muon_multi_step with the same values.  Values
+ * are checked on the device: a non-finite value, or mu or beta2 outside [0, 1],
+ * makes mb_sync_status return MB_ERR_ARG and leaves the step's outputs undefined.
+ * Host-side errors as for muon_multi_step; MB_ERR_NULL / MB_ERR_ALIGN for
+ * scalars_dev.  One more (single-block) launch than muon_multi_step. */
+int muon_multi_step_dev(const mb_bank_desc* banks, int n_banks, const float* scalars_dev,
+                        int normuon, int ns_steps, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream);
+
 /* ---- single stages, for callers that run them separately (and for tests) ---- */
 
 /* S1 only: momentum in place and u (bf16 [batch, rows, cols], dense) out. */
@@ -177,7 +193,8 @@ int mb_workspace_views(mb_shape shape, int normuon, int ns_steps, size_t* u_offs
                        size_t* v_offset, size_t* row_pitch);
 
 /* Synchronises `cuda_stream`, then returns and clears this device's latched
- * device-side status (MB_OK or MB_ERR_TIMEOUT), or MB_ERR_CUDA. */
+ * device-side status (MB_OK, MB_ERR_TIMEOUT, or MB_ERR_ARG for a bad scalar
+ * read by muon_multi_step_dev), or MB_ERR_CUDA. */
 int mb_sync_status(void* cuda_stream);
 
 /* Runs the bounded-wait primitive of the kernels against an mbarrier that

@@ -139,6 +139,25 @@ def muon_multi_step(banks: Sequence[BankState], lr: float, wd: float, mu: float,
     return ws
 
 
+def muon_multi_step_dev(banks: Sequence[BankState], scalars, normuon: bool = False, ns_steps: int = 5,
+                        workspace=None, stream=None):
+    """muon_multi_step with the hyperparameters read on the device from `scalars`.
+
+    `scalars` is a CUDA float32 tensor of len(banks) x 4 values (lr, wd, mu, beta2 per bank).
+    The step reads it when it runs, so a CUDA graph that captured this call replays
+    with whatever the tensor holds at replay time.
+    """
+    if not (isinstance(scalars, torch.Tensor) and scalars.is_cuda and scalars.dtype == torch.float32
+            and scalars.is_contiguous() and scalars.numel() == 4 * len(banks)):
+        raise ValueError("scalars must be a contiguous CUDA float32 tensor of 4 values per bank")
+    arr = _descs(banks)
+    ws = _workspace(mb_multi_workspace_bytes(banks, normuon), workspace, banks[0].bank.device)
+    st = _b.load().muon_multi_step_dev(arr, len(banks), scalars.data_ptr(), int(normuon), ns_steps, ws.data_ptr(),
+                                       ws.numel() * ws.element_size(), _stream(stream))
+    _b.check("muon_multi_step_dev", st)
+    return ws
+
+
 def mb_momentum(grad, momentum, u, mu: float, stream=None):
     sh = _shape(grad)
     _b.check("mb_momentum", _b.load().mb_momentum(

@@ -49,6 +49,7 @@ _SIGNATURES = {
     "mb_multi_workspace_bytes": (c_int, [ctypes.POINTER(MbBankDesc), c_int, c_int, ctypes.POINTER(c_size_t)]),
     "muon_multi_step": (c_int, [ctypes.POINTER(MbBankDesc), c_int, c_float, c_float, c_float, c_int, c_float,
                                 c_int, _P, c_size_t, _P]),
+    "muon_multi_step_dev": (c_int, [ctypes.POINTER(MbBankDesc), c_int, _P, c_int, c_int, _P, c_size_t, _P]),
     "mb_momentum": (c_int, [_P, _P, _P, MbShape, c_float, _P]),
     "mb_newton_schulz": (c_int, [_P, _P, MbShape, c_int, _P, c_size_t, _P]),
     "mb_newton_schulz_noalloc": (c_int, [_P, _P, MbShape, c_int, _P]),

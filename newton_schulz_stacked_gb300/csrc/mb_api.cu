@@ -164,6 +164,7 @@ struct Layout {
   int batch, rows, cols, m, n, tall, small, ld, ldm, P;
   size_t x[3], a, b, xf[2], partials, scale, q, rowscale;  // x[0] = u, x[1], x[2] = iterates
   size_t sync, sync_bytes;   // large banks: NS completion counters, then the task counter
+  size_t dscal;              // derived scalars of a step with device-memory hyperparameters
   size_t end;
 };
 
@@ -199,6 +200,7 @@ Layout make_layout(const mb_shape& s, int normuon, size_t base) {
     L.xf[0] = take(B * E * 4);
     L.xf[1] = take(B * E * 4);
   }
+  L.dscal = take(DSCAL_COUNT * sizeof(float));
   L.partials = take(B * L.P * 4);
   L.scale = take(B * 4);
   if (normuon) {
@@ -294,12 +296,14 @@ EwParams ew_params(const Bank* banks, int nb, Fill fill) {
 
 // S1 (+ S2 partials): u into x[0]; `src_dense` replaces the gradient with a
 // ready u when `momentum` is false (the stand-alone NS entry point).
-int stage_k1(const Bank* b, int nb, bool momentum, float mu, cudaStream_t st, DeviceState* ds) {
+int stage_k1(const Bank* b, int nb, bool momentum, float mu, cudaStream_t st, DeviceState* ds,
+             bool dev_scalars = false) {
   EwParams p = ew_params(b, nb, [&](const Bank& k, EwBank& e) {
     e.src = k.grad;
     e.mom = k.mom;
     e.xout = k.at<uint16_t>(k.L.x[0]);
     e.partials = k.at<float>(k.L.partials);
+    e.dscal = dev_scalars ? k.at<float>(k.L.dscal) : nullptr;
   });
   p.mu = mu;
   p.omm = static_cast<float>(1.0 - static_cast<double>(mu));
@@ -465,7 +469,8 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
 }
 
 // S6 statistics: per-row factor into rowscale, state in place; v with pitch `vld`.
-int stage_normuon(const Bank* b, int nb, float beta2, const uint16_t* const* v, const int* vld, cudaStream_t st) {
+int stage_normuon(const Bank* b, int nb, float beta2, const uint16_t* const* v, const int* vld, cudaStream_t st,
+                  bool dev_scalars = false) {
   RowParams rp{};
   rp.nb = nb;
   rp.beta2 = beta2;
@@ -483,6 +488,7 @@ int stage_normuon(const Bank* b, int nb, float beta2, const uint16_t* const* v, 
     r.ld = vld[i];
     r.row_begin = rows;
     r.mat_begin = mats;
+    r.dscal = dev_scalars ? b[i].at<float>(L.dscal) : nullptr;
     rows += L.batch * L.rows;
     mats += L.batch;
   }
@@ -494,15 +500,19 @@ int stage_normuon(const Bank* b, int nb, float beta2, const uint16_t* const* v, 
 }
 
 // S5: update from v (pitch vld); NorMuon uses the per-row factors.
+// sqrt(max(1, rows / cols)): the shape factor of the learning rate ("Muon Custom Sizing", section 4).
+double shape_factor(const Layout& L) { return std::sqrt(std::fmax(1.0, static_cast<double>(L.rows) / L.cols)); }
+
 int stage_k3(const Bank* b, int nb, bool normuon, float lr, float wd, const uint16_t* const* v, const int* vld,
-             cudaStream_t st) {
+             cudaStream_t st, bool dev_scalars = false) {
   EwParams p = ew_params(b, nb, [&](const Bank& k, EwBank& e) {
     e.bank = k.bank;
     e.mant = k.mant;
     e.rowscale = normuon ? k.at<float>(k.L.rowscale) : nullptr;
     const double lrd = lr, wdd = wd;
-    e.decay = static_cast<float>(1.0 - lrd * wdd);
-    e.neg_lr = static_cast<float>(-lrd * std::sqrt(std::fmax(1.0, static_cast<double>(k.L.rows) / k.L.cols)));
+    e.decay = static_cast<float>(std::fma(-lrd, wdd, 1.0));   // 1 - lr*wd, rounded once
+    e.neg_lr = static_cast<float>(-lrd * shape_factor(k.L));
+    e.dscal = dev_scalars ? k.at<float>(k.L.dscal) : nullptr;
   });
   for (int i = 0; i < nb; ++i) {
     p.b[i].xin = v[i];
@@ -541,12 +551,16 @@ int check_workspace(void* ws, size_t have, size_t need) {
   return MB_OK;
 }
 
+// One step over nb banks.  With `scalars_dev` the hyperparameters are read from
+// device memory when the step runs ({lr, wd, mu, beta2} per bank) and lr..beta2
+// are ignored.
 int run_step(const mb_bank_desc* d, int nb, float lr, float wd, float mu, int normuon, float beta2, int ns_steps,
-             void* workspace, size_t ws_bytes, void* stream) {
+             void* workspace, size_t ws_bytes, void* stream, const float* scalars_dev = nullptr) {
   if (!d) return MB_ERR_NULL;
   if (nb <= 0 || nb > MAX_BANKS) return nb <= 0 ? MB_ERR_ARG : MB_ERR_TOO_MANY;
   if (ns_steps < 0 || ns_steps > MAX_NS_STEPS) return MB_ERR_NS_STEPS;
-  MB_TRY(check_scalars(lr, wd, mu, normuon ? beta2 : 0.f));
+  const bool dev = scalars_dev != nullptr;
+  if (!dev) MB_TRY(check_scalars(lr, wd, mu, normuon ? beta2 : 0.f));
   for (int i = 0; i < nb; ++i) MB_TRY(validate_bank(d[i], normuon));
   Layout L[MAX_BANKS];
   size_t need = 0;
@@ -570,10 +584,25 @@ int run_step(const mb_bank_desc* d, int nb, float lr, float wd, float mu, int no
     vld[i] = L[i].ld;
   }
   mark(MB_MARK_BEGIN, st);
-  MB_TRY(stage_k1(b, nb, true, mu, st, ds));
+  if (dev) {
+    // the derived scalars of every bank, read from the caller's buffer as this step runs
+    // (timed with the momentum stage)
+    ScalarParams sp{};
+    sp.nb = nb;
+    sp.normuon = normuon;
+    sp.status = ds->status;
+    for (int i = 0; i < nb; ++i) {
+      sp.b[i].src = scalars_dev + 4 * i;
+      sp.b[i].dst = b[i].at<float>(L[i].dscal);
+      sp.b[i].shape_factor = shape_factor(L[i]);
+    }
+    MB_TRY_CUDA(launch_scalars(sp, st));
+    ++g_launch_count;
+  }
+  MB_TRY(stage_k1(b, nb, true, mu, st, ds, dev));
   MB_TRY(stage_ns(b, nb, ns_steps, st, ds));
-  if (normuon) MB_TRY(stage_normuon(b, nb, beta2, v, vld, st));
-  MB_TRY(stage_k3(b, nb, normuon != 0, lr, wd, v, vld, st));
+  if (normuon) MB_TRY(stage_normuon(b, nb, beta2, v, vld, st, dev));
+  MB_TRY(stage_k3(b, nb, normuon != 0, lr, wd, v, vld, st, dev));
   return MB_OK;
 }
 
@@ -640,6 +669,14 @@ int muon_multi_step(const mb_bank_desc* banks, int n_banks, float lr, float wd, 
                     float beta2, int ns_steps, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return run_step(banks, n_banks, lr, wd, mu, normuon ? 1 : 0, beta2, ns_steps, workspace, workspace_bytes,
                   cuda_stream);
+}
+
+int muon_multi_step_dev(const mb_bank_desc* banks, int n_banks, const float* scalars_dev, int normuon,
+                        int ns_steps, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!scalars_dev) return MB_ERR_NULL;
+  if (!aligned16(scalars_dev)) return MB_ERR_ALIGN;
+  return run_step(banks, n_banks, 0.f, 0.f, 0.f, normuon ? 1 : 0, 0.f, ns_steps, workspace, workspace_bytes,
+                  cuda_stream, scalars_dev);
 }
 
 int mb_momentum(const void* grad_bf16, float* momentum_f32, void* u_bf16, mb_shape shape, float mu,
@@ -764,7 +801,7 @@ int mb_sync_status(void* cuda_stream) {
   MB_TRY_CUDA(cudaMemcpy(&h, ds->status, sizeof(int), cudaMemcpyDeviceToHost));
   const int zero = 0;
   MB_TRY_CUDA(cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice));
-  return h == DEV_OK ? MB_OK : MB_ERR_TIMEOUT;
+  return h == DEV_OK ? MB_OK : h == DEV_BAD_SCALAR ? MB_ERR_ARG : MB_ERR_TIMEOUT;
 }
 
 int mb_selftest_timeout(unsigned limit_us, void* cuda_stream) {

@@ -12,6 +12,7 @@ namespace mb {
 // Device status word values (latched by the kernels, read by mb_sync_status).
 constexpr int DEV_OK = 0;
 constexpr int DEV_TIMEOUT = 1;
+constexpr int DEV_BAD_SCALAR = 3;  // a hyperparameter read from device memory is not finite or out of range
 
 // A wait that has not completed after this long is treated as a fault.
 constexpr uint64_t WAIT_LIMIT_NS = 1000ull * 1000ull * 1000ull;  // 1 s

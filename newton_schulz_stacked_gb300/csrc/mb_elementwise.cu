@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(EW_THREADS) k1_kernel(const __grid_constant__ 
   const uint16_t* src = B.src + moff;
   float* mom = MOMENTUM ? B.mom + moff : nullptr;
   uint16_t* xo = B.xout + static_cast<size_t>(mat) * B.rows * B.out_ld;
-  const float mu = p.mu, omm = p.omm;
+  const float mu = B.dscal ? B.dscal[DSCAL_MU] : p.mu, omm = B.dscal ? B.dscal[DSCAL_OMM] : p.omm;
   float ss = 0.f;
 
   auto step = [&](float g, float& b) -> float {
@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(256) row_scale_kernel(const __grid_constant__ 
   const int mat = blockIdx.x - B.mat_begin;
   const size_t base = static_cast<size_t>(mat) * B.rows;
   const float inv_cols = 1.0f / static_cast<float>(B.cols);
-  const float b2 = p.beta2, omb2 = 1.0f - p.beta2;
+  const float beta2 = B.dscal ? B.dscal[DSCAL_BETA2] : p.beta2;
+  const float b2 = beta2, omb2 = 1.0f - beta2;
   float nv = 0.f, nh = 0.f;
   for (int r = threadIdx.x; r < B.rows; r += 256) {
     const float q = B.q[base + r];
@@ -366,7 +367,8 @@ __global__ void __launch_bounds__(EW_THREADS) k3_kernel(const __grid_constant__ 
   uint16_t* mb_ = B.mant + moff;
   const uint16_t* v = B.xin + static_cast<size_t>(mat) * B.rows * B.ld;
   const float* rs = NORMUON ? B.rowscale + static_cast<size_t>(mat) * B.rows : nullptr;
-  const float decay = B.decay, neg_lr = B.neg_lr;
+  const float decay = B.dscal ? B.dscal[DSCAL_DECAY] : B.decay;
+  const float neg_lr = B.dscal ? B.dscal[DSCAL_NEG_LR] : B.neg_lr;
   if ((B.cols & 7) == 0) {
     for (int e = e0 + threadIdx.x * 8; e < e1; e += EW_THREADS * 8) {
       const int row = e / B.cols, col = e - row * B.cols;
@@ -494,6 +496,33 @@ cudaError_t launch_k3(const EwParams& p, bool normuon, cudaStream_t s) {
     k3_kernel<true><<<p.total_blocks, EW_THREADS, 0, s>>>(p);
   else
     k3_kernel<false><<<p.total_blocks, EW_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// The derived scalars of a step whose hyperparameters sit in device memory: one
+// thread per bank forms, in double and rounded once to fp32, exactly what the
+// host forms for the by-value calls (1 - mu; 1 - lr*wd as one fused operation;
+// -lr times the shape factor), so both kinds of call give identical bits.  An
+// invalid value latches DEV_BAD_SCALAR; the step still runs on what it read.
+__global__ void scalars_kernel(const __grid_constant__ ScalarParams p) {
+  const int i = threadIdx.x;
+  if (i >= p.nb) return;
+  const ScalarBank& B = p.b[i];
+  const float lr = B.src[0], wd = B.src[1], mu = B.src[2], beta2 = B.src[3];
+  const bool ok = isfinite(lr) && isfinite(wd) && isfinite(mu) && mu >= 0.f && mu <= 1.f &&
+                  (!p.normuon || (isfinite(beta2) && beta2 >= 0.f && beta2 <= 1.f));
+  if (!ok) latch_status(p.status, DEV_BAD_SCALAR);
+  const double lrd = lr, wdd = wd;
+  B.dst[DSCAL_MU] = mu;
+  B.dst[DSCAL_OMM] = static_cast<float>(__dsub_rn(1.0, static_cast<double>(mu)));
+  B.dst[DSCAL_DECAY] = static_cast<float>(fma(-lrd, wdd, 1.0));
+  B.dst[DSCAL_NEG_LR] = static_cast<float>(__dmul_rn(-lrd, B.shape_factor));
+  B.dst[DSCAL_BETA2] = beta2;
+}
+
+cudaError_t launch_scalars(const ScalarParams& p, cudaStream_t s) {
+  if (p.nb <= 0) return cudaSuccess;
+  scalars_kernel<<<1, 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -31,6 +31,22 @@ struct EwBank {
   int P;                   // chunks per matrix
   int block_begin;         // first block of this bank in the launch
   float decay, neg_lr;     // K3: 1 - lr*wd, -lr*sqrt(max(1, rows/cols))
+  const float* dscal;      // this bank's scalars in device memory (DSCAL_* order), or null: use the fields above
+};
+
+// Derived per-bank scalars of a step whose hyperparameters are read from device
+// memory (muon_multi_step_dev), in the workspace: the values the host forms in
+// double for the by-value calls, formed the same way by scalars_kernel.
+enum DerivedScalar { DSCAL_MU = 0, DSCAL_OMM, DSCAL_DECAY, DSCAL_NEG_LR, DSCAL_BETA2, DSCAL_COUNT = 8 };
+struct ScalarBank {
+  const float* src;        // caller's {lr, wd, mu, beta2} of this bank
+  float* dst;              // DSCAL_COUNT derived values
+  double shape_factor;     // sqrt(max(1, rows / cols)), formed on the host
+};
+struct ScalarParams {
+  ScalarBank b[MAX_BANKS];
+  int nb, normuon;
+  int* status;
 };
 
 struct EwParams {
@@ -77,6 +93,7 @@ struct RowBank {
   int batch, rows, cols, ld;
   int row_begin;        // prefix over rows (KN1) ...
   int mat_begin;        // ... and over matrices (KN2)
+  const float* dscal;   // derived scalars in device memory, or null: use RowParams::beta2
 };
 struct RowParams {
   RowBank b[MAX_BANKS];
@@ -140,6 +157,7 @@ cudaError_t launch_small_ns(const SmallParams& p, bool in_smem, cudaStream_t s);
 cudaError_t launch_row_sumsq(const RowParams& p, cudaStream_t s);
 cudaError_t launch_row_scale(const RowParams& p, cudaStream_t s);
 cudaError_t launch_k3(const EwParams& p, bool normuon, cudaStream_t s);
+cudaError_t launch_scalars(const ScalarParams& p, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_ns_fused(const NsParams& p, cudaStream_t s);
 

@@ -125,6 +125,12 @@ def test_multi_step_argument_errors(lib):
     assert lib.muon_multi_step(None, 1, 0.02, 0.01, 0.95, 0, 0.95, 5, good, 1 << 30, None) == b.MB_ERR_NULL
     # normuon over banks without row state
     assert lib.muon_multi_step(arr, 2, 0.02, 0.01, 0.95, 1, 0.95, 5, good, 1 << 30, None) == b.MB_ERR_NULL
+    # device-memory hyperparameters: the buffer pointer is checked before anything else
+    assert lib.muon_multi_step_dev(arr, 2, None, 0, 5, good, 1 << 30, None) == b.MB_ERR_NULL
+    assert lib.muon_multi_step_dev(arr, 2, good + 4, 0, 5, good, 1 << 30, None) == b.MB_ERR_ALIGN
+    assert lib.muon_multi_step_dev(arr, 9, good, 0, 5, good, 1 << 30, None) == b.MB_ERR_TOO_MANY
+    assert lib.muon_multi_step_dev(arr, 2, good, 0, 17, good, 1 << 30, None) == b.MB_ERR_NS_STEPS
+    assert lib.muon_multi_step_dev(arr, 2, good, 1, 5, good, 1 << 30, None) == b.MB_ERR_NULL
 
 
 def test_stage_argument_errors(lib):
