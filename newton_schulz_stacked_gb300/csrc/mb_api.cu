@@ -423,7 +423,6 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
       MB_TRY(encode_map(&nb_.st_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       MB_TRY(encode_map(&nb_.st_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       nb_.a = k.at<uint16_t>(L.a);
-      nb_.b = k.at<uint16_t>(L.b);
       nb_.x_ld = L.ld;
       nb_.x_ms = static_cast<long long>(L.rows) * L.ld;
       nb_.m_ld = L.ldm;

@@ -119,9 +119,8 @@ struct NsBank {
   CUtensorMap xmn2[3], xmn4[3];     // X buffers, MN-major boxes of 64 K rows x 128 and 256 columns
   CUtensorMap ak, ak2, bk, bk2;     // A and B, K-major boxes of 128 and 256 rows x 64
   CUtensorMap st_x[3], st_a, st_b;  // 32x32 store boxes (64-byte swizzle)
-  uint16_t* x[3];                   // X buffers (epilogue inputs and direct stores)
-  uint16_t* a;                      // A and B (direct stores; A is POLY's epilogue input)
-  uint16_t* b;
+  const uint16_t* x[3];             // X buffers (APPLY's epilogue input)
+  const uint16_t* a;                // A (POLY's epilogue input)
   long long x_ld, x_ms, m_ld, m_ms;  // pitches (elements) and matrix strides
   const float* scale;               // per-matrix 1/(||u||_F + eps)
   unsigned* done;                   // completion counters [batch][MAX_NS_STEPS][3], zeroed before launch

@@ -230,6 +230,29 @@ def test_multi_step_equals_single_steps(nss):
         np.testing.assert_array_equal(f32(a.momentum), f32(b.momentum))
 
 
+def test_step_on_a_caller_stream(nss):
+    """The step is ordered on the stream it is given, including the fp32 gate banks that run on the
+    library's side stream (forked from and joined back to the caller's stream)."""
+    shapes = [(4, 256, 384), (1, 12, 768), (10, 6, 12)]
+    states = [_case(60 + i, s) for i, s in enumerate(shapes)]
+    ref = [nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant)) for (w, mant, mom, row, g) in states]
+    nss.muon_multi_step(ref, LR, WD, MU, ns_steps=5)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        # the inputs are made on the caller's stream, and the step follows them there
+        banks = [nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant))
+                 for (w, mant, mom, row, g) in states]
+        nss.muon_multi_step(banks, LR, WD, MU, ns_steps=5, stream=side)
+        out = [(b.bank.clone(), b.mantissa.clone(), b.momentum.clone()) for b in banks]
+    side.synchronize()
+    assert nss.mb_sync_status(side) == 0
+    for (bank, mant, mom), r in zip(out, ref):
+        np.testing.assert_array_equal(u16(bank), u16(r.bank))
+        np.testing.assert_array_equal(u16(mant), u16(r.mantissa))
+        np.testing.assert_array_equal(f32(mom), f32(r.momentum))
+
+
 def test_deterministic(nss):
     shape = (3, 512, 256)
     outs = []
