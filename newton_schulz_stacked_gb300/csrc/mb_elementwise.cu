@@ -13,6 +13,8 @@
 //   k3_kernel      S5 mixed-precision update (Track-2 record 7 write-up,
 //                  section 4.1): fp32 from bf16 + mantissa, decay, scaled
 //                  step, truncating split.
+#include <atomic>
+
 #include "mb_device.cuh"
 #include "mb_internal.h"
 
@@ -462,12 +464,13 @@ cudaError_t launch_small_ns(const SmallParams& p, bool in_smem, cudaStream_t s) 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool attr_done[64];
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+  // set once per device; concurrent first calls from several host threads set it alike
+  static std::atomic<bool> attr_done[64];
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(reinterpret_cast<const void*>(small_ns_kernel<true>),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SMEM_MAX);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   int bytes = 0;
   for (int i = 0; i < p.nb; ++i) {

@@ -39,6 +39,8 @@
 //   warps 2..9    : epilogue, two warps per 32-lane TMEM quadrant (each takes
 //                   half the columns); task k's epilogue runs under task k+1's
 //                   MMAs; results leave through shared memory by TMA bulk stores
+#include <atomic>
+
 #include "mb_device.cuh"
 #include "mb_internal.h"
 
@@ -688,8 +690,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
   }
 }
 
-bool g_attr_done[64];
-int g_num_sms[64];
+// per-device launch set-up, done by the first call on each device (concurrent first calls
+// from several host threads do the same idempotent work)
+std::atomic<bool> g_attr_done[64];
+std::atomic<int> g_num_sms[64];
 
 }  // namespace
 
@@ -699,17 +703,19 @@ cudaError_t launch_ns_fused(const NsParams& p, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!g_attr_done[dev]) {
+  if (!g_attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(reinterpret_cast<const void*>(ns_fused_kernel),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
     if (e != cudaSuccess) return e;
-    g_attr_done[dev] = true;
+    g_attr_done[dev].store(true, std::memory_order_release);
   }
-  if (g_num_sms[dev] == 0) {
-    e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  int nsm = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (nsm == 0) {
+    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    g_num_sms[dev].store(nsm, std::memory_order_relaxed);
   }
-  const int grid = p.total_tasks < g_num_sms[dev] ? p.total_tasks : g_num_sms[dev];
+  const int grid = p.total_tasks < nsm ? p.total_tasks : nsm;
   ns_fused_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p);
   return cudaGetLastError();
 }

@@ -253,6 +253,47 @@ def test_step_on_a_caller_stream(nss):
         np.testing.assert_array_equal(f32(mom), f32(r.momentum))
 
 
+def test_concurrent_host_threads(nss):
+    """Two host threads step their own banks on their own streams at the same time (the C calls
+    release the GIL); each result matches the same steps run one after the other."""
+    import threading
+    shapes = [[(4, 256, 384), (10, 6, 12)], [(3, 384, 256), (1, 12, 768)]]
+    states = [[_case(80 + 10 * t + i, s) for i, s in enumerate(sh)] for t, sh in enumerate(shapes)]
+
+    def banks_of(st):
+        return [nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant)) for (w, mant, mom, row, g) in st]
+
+    ref = [banks_of(st) for st in states]
+    for banks in ref:
+        for _ in range(3):
+            nss.muon_multi_step(banks, LR, WD, MU, ns_steps=5)
+    torch.cuda.synchronize()
+    out, errors = [None, None], []
+
+    def run(t):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                banks = banks_of(states[t])
+                for _ in range(3):
+                    nss.muon_multi_step(banks, LR, WD, MU, ns_steps=5, stream=stream)
+                out[t] = [(u16(b.bank), u16(b.mantissa)) for b in banks]
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert nss.mb_sync_status() == 0
+    for t in range(2):
+        for (bank, mant), r in zip(out[t], ref[t]):
+            np.testing.assert_array_equal(bank, u16(r.bank))
+            np.testing.assert_array_equal(mant, u16(r.mantissa))
+
+
 def test_deterministic(nss):
     shape = (3, 512, 256)
     outs = []
