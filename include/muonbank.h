@@ -151,6 +151,18 @@ int mb_momentum(const void* grad_bf16, float* momentum_f32, void* u_bf16, mb_sha
 int mb_newton_schulz(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps,
                      void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* mb_newton_schulz with a coefficient schedule: step i uses (a, b, c) =
+ * coeffs[3i], coeffs[3i+1], coeffs[3i+2] instead of the quintic (3.4445, -4.7750,
+ * 2.0315) that every other call uses for every step ("Muon Custom Sizing",
+ * section 2.3).  For per-iteration schedules such as the Polar Express
+ * orthogonalisation named in the "Unified zero-copy optimizer" write-up (section 4),
+ * whose coefficients the pages do not print.  coeffs: host array of 3 * ns_steps
+ * finite floats, read during the call.  MB_ERR_NULL / MB_ERR_ARG for coeffs, other
+ * errors as mb_newton_schulz.  The bf16 tolerance of the result depends on the schedule. */
+int mb_newton_schulz_coeffs(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps,
+                            const float* coeffs, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream);
+
 /* S2-S4 like mb_newton_schulz, for callers that cannot allocate device memory.
  *
  * Not part of the method on the speedrun pages (they have no counterpart);

@@ -165,6 +165,22 @@ def mb_momentum(grad, momentum, u, mu: float, stream=None):
         mu, _stream(stream)))
 
 
+def mb_newton_schulz_coeffs(u, v, coeffs, workspace=None, stream=None):
+    """mb_newton_schulz with a per-step coefficient schedule: `coeffs` is a sequence of
+    (a, b, c), one per step (its length is the number of steps)."""
+    import ctypes
+    flat = [float(x) for abc in coeffs for x in abc]
+    if len(flat) != 3 * len(coeffs):
+        raise ValueError("coeffs must be a sequence of (a, b, c) triples")
+    arr = (ctypes.c_float * max(len(flat), 1))(*flat)
+    sh = _shape(u)
+    ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols)), workspace, u.device)
+    _b.check("mb_newton_schulz_coeffs", _b.load().mb_newton_schulz_coeffs(
+        _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, len(coeffs), arr, ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return ws
+
+
 def mb_newton_schulz(u, v, ns_steps: int = 5, workspace=None, stream=None):
     sh = _shape(u)
     ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols)), workspace, u.device)

@@ -52,6 +52,7 @@ _SIGNATURES = {
     "muon_multi_step_dev": (c_int, [ctypes.POINTER(MbBankDesc), c_int, _P, c_int, c_int, _P, c_size_t, _P]),
     "mb_momentum": (c_int, [_P, _P, _P, MbShape, c_float, _P]),
     "mb_newton_schulz": (c_int, [_P, _P, MbShape, c_int, _P, c_size_t, _P]),
+    "mb_newton_schulz_coeffs": (c_int, [_P, _P, MbShape, c_int, ctypes.POINTER(c_float), _P, c_size_t, _P]),
     "mb_newton_schulz_noalloc": (c_int, [_P, _P, MbShape, c_int, _P]),
     "mb_update": (c_int, [_P, _P, _P, MbShape, c_float, c_float, _P]),
     "mb_normuon_update": (c_int, [_P, _P, _P, _P, MbShape, c_float, c_float, c_float, _P, c_size_t, _P]),

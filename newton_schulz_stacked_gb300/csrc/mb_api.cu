@@ -325,8 +325,20 @@ int stage_k1(const Bank* b, int nb, bool momentum, float mu, cudaStream_t st, De
   return MB_OK;
 }
 
+// Each step's (a, b, c): coeffs[3 i .. 3 i + 2] for step i, or the quintic of the pages
+// ("Muon Custom Sizing", section 2.3) for every step when coeffs is null.
+void set_coeffs(float* ca, float* cb, float* cc, int steps, const float* coeffs) {
+  for (int i = 0; i < MAX_NS_STEPS; ++i) {
+    const bool own = coeffs && i < steps;
+    ca[i] = own ? coeffs[3 * i] : NS_A;
+    cb[i] = own ? coeffs[3 * i + 1] : NS_B;
+    cc[i] = own ? coeffs[3 * i + 2] : NS_C;
+  }
+}
+
 // S3-S4 for every bank: the result lands in x[final_buffer(steps)].
-int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds) {
+int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds,
+             const float* coeffs = nullptr) {
   if (steps == 0) {
     EwParams p = ew_params(b, nb, [&](const Bank& k, EwBank& e) {
       e.xin = k.at<uint16_t>(k.L.x[0]);
@@ -352,9 +364,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     const bool in_smem = pass == 0;
     SmallParams sp{};
     sp.steps = steps;
-    sp.ca = NS_A;
-    sp.cb = NS_B;
-    sp.cc = NS_C;
+    set_coeffs(sp.ca, sp.cb, sp.cc, steps, coeffs);
     int blocks = 0, n = 0;
     for (int i = 0; i < nb; ++i) {
       const Layout& L = b[i].L;
@@ -399,9 +409,7 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds)
     NsParams np{};
     np.nbank = gn;
     np.steps = steps;
-    np.ca = NS_A;
-    np.cb = NS_B;
-    np.cc = NS_C;
+    set_coeffs(np.ca, np.cb, np.cc, steps, coeffs);
     np.status = ds->status;
     for (int j = 0; j < gn; ++j) {
       const Bank& k = b[large[g0 + j]];
@@ -605,6 +613,34 @@ int run_step(const mb_bank_desc* d, int nb, float lr, float wd, float mu, int no
   return MB_OK;
 }
 
+// S2-S4 as a stage of its own: u (dense, bf16) in, v (dense, bf16) out.
+int ns_stage(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps, const float* coeffs, void* workspace,
+             size_t workspace_bytes, void* cuda_stream) {
+  MB_TRY(check_shape(shape));
+  MB_TRY(check_ptr(u_bf16));
+  MB_TRY(check_ptr(v_bf16));
+  if (ns_steps < 0 || ns_steps > MAX_NS_STEPS) return MB_ERR_NS_STEPS;
+  const Layout L = make_layout(shape, 0, 0);
+  MB_TRY(check_workspace(workspace, workspace_bytes, L.end));
+  DeviceState* ds = nullptr;
+  MB_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  Bank k{};
+  k.grad = static_cast<const uint16_t*>(u_bf16);
+  k.L = L;
+  k.ws = static_cast<uint8_t*>(workspace);
+  mark(MB_MARK_BEGIN, st);
+  MB_TRY(stage_k1(&k, 1, false, 0.f, st, ds));
+  MB_TRY(stage_ns(&k, 1, ns_steps, st, ds, coeffs));
+  EwParams p = ew_params(&k, 1, [&](const Bank& bk, EwBank& e) {
+    e.xin = bk.at<uint16_t>(bk.L.x[final_buffer(ns_steps)]);
+    e.xout = static_cast<uint16_t*>(v_bf16);
+    e.out_ld = bk.L.cols;
+  });
+  MB_LAUNCH(launch_unpack(p, st), p.total_blocks > 0, MB_MARK_NS0, st);
+  return MB_OK;
+}
+
 }  // namespace
 }  // namespace mb
 
@@ -709,29 +745,16 @@ int mb_momentum(const void* grad_bf16, float* momentum_f32, void* u_bf16, mb_sha
 
 int mb_newton_schulz(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps, void* workspace,
                      size_t workspace_bytes, void* cuda_stream) {
-  MB_TRY(check_shape(shape));
-  MB_TRY(check_ptr(u_bf16));
-  MB_TRY(check_ptr(v_bf16));
+  return ns_stage(u_bf16, v_bf16, shape, ns_steps, nullptr, workspace, workspace_bytes, cuda_stream);
+}
+
+int mb_newton_schulz_coeffs(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps, const float* coeffs,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!coeffs) return MB_ERR_NULL;
   if (ns_steps < 0 || ns_steps > MAX_NS_STEPS) return MB_ERR_NS_STEPS;
-  const Layout L = make_layout(shape, 0, 0);
-  MB_TRY(check_workspace(workspace, workspace_bytes, L.end));
-  DeviceState* ds = nullptr;
-  MB_TRY(device_state(&ds));
-  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  Bank k{};
-  k.grad = static_cast<const uint16_t*>(u_bf16);
-  k.L = L;
-  k.ws = static_cast<uint8_t*>(workspace);
-  mark(MB_MARK_BEGIN, st);
-  MB_TRY(stage_k1(&k, 1, false, 0.f, st, ds));
-  MB_TRY(stage_ns(&k, 1, ns_steps, st, ds));
-  EwParams p = ew_params(&k, 1, [&](const Bank& bk, EwBank& e) {
-    e.xin = bk.at<uint16_t>(bk.L.x[final_buffer(ns_steps)]);
-    e.xout = static_cast<uint16_t*>(v_bf16);
-    e.out_ld = bk.L.cols;
-  });
-  MB_LAUNCH(launch_unpack(p, st), p.total_blocks > 0, MB_MARK_NS0, st);
-  return MB_OK;
+  for (int i = 0; i < 3 * ns_steps; ++i)
+    if (!std::isfinite(coeffs[i])) return MB_ERR_ARG;
+  return ns_stage(u_bf16, v_bf16, shape, ns_steps, coeffs, workspace, workspace_bytes, cuda_stream);
 }
 
 int mb_update(void* bank_bf16, uint16_t* mantissa, const void* v_bf16, mb_shape shape, float lr, float wd,

@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(SMALL_THREADS) small_ns_kernel(const __grid_co
       const int i = e / m, j = e - i * m;
       float acc = 0.f;
       for (int l = 0; l < m; ++l) acc = fmaf(sA[i * m + l], sA[l * m + j], acc);
-      sB[e] = p.cb * sA[e] + p.cc * acc;
+      sB[e] = p.cb[it] * sA[e] + p.cc[it] * acc;
     }
     __syncthreads();
     // X <- a X + B X, written in the stored orientation
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(SMALL_THREADS) small_ns_kernel(const __grid_co
       } else {     // logical (i = r, k = c): sum_j B[r][j] stored(j, c)
         for (int j = 0; j < m; ++j) acc = fmaf(sB[r * m + j], cur[static_cast<size_t>(j) * cols + c], acc);
       }
-      nxt[e] = fmaf(p.ca, cur[e], acc);
+      nxt[e] = fmaf(p.ca[it], cur[e], acc);
     }
     __syncthreads();
   }

@@ -10,6 +10,7 @@ namespace mb {
 
 constexpr int MAX_BANKS = 8;       // banks per element-wise launch
 constexpr int SMALL_M = 64;        // min(rows, cols) <= SMALL_M: fp32 SIMT Newton-Schulz
+constexpr int MAX_NS_STEPS = 16;   // Newton-Schulz steps one call accepts
 
 // Elements handled by one block of the element-wise kernels (per matrix chunk).
 constexpr int EW_THREADS = 256;
@@ -81,7 +82,7 @@ struct SmallBank {
 struct SmallParams {
   SmallBank b[MAX_BANKS];
   int nb, total_blocks, steps;
-  float ca, cb, cc;
+  float ca[MAX_NS_STEPS], cb[MAX_NS_STEPS], cc[MAX_NS_STEPS];   // (a, b, c) of each step
 };
 
 // NorMuon row statistics and scales.
@@ -106,7 +107,6 @@ struct RowParams {
 enum GemmEpi { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2 };   // the three GEMM phases of one step
 
 constexpr int MAX_NS_BANKS = 4;     // large banks per fused Newton-Schulz launch
-constexpr int MAX_NS_STEPS = 16;
 
 // One large bank in the fused Newton-Schulz launch.  x[0] holds u; the
 // iterates X_1, X_2, ... alternate between x[1] and x[2].
@@ -138,7 +138,7 @@ struct NsParams {
   unsigned char seg_bank[3 * MAX_NS_BANKS], seg_ph[3 * MAX_NS_BANKS];
   int tasks_per_iter, total_tasks;
   unsigned* next_task;              // dynamic scheduler, zeroed before launch
-  float ca, cb, cc;
+  float ca[MAX_NS_STEPS], cb[MAX_NS_STEPS], cc[MAX_NS_STEPS];   // (a, b, c) of each step
   int* status;
 };
 

@@ -245,6 +245,7 @@ struct EpiJob {
   const CUtensorMap* st_lo;
   const uint16_t* ein_lo;
   int M, N, sym, mat, m0, n0, nt;
+  int it;                  // Newton-Schulz step: picks its (a, b, c)
   float alpha;
 };
 
@@ -276,6 +277,7 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
   const bool odd = lane & 1;
   const uint32_t word_off = 4u * ((lane >> 1) & 3);
+  const float ca = P.ca[J.it], cb = P.cb[J.it], cc = P.cc[J.it];
 
   uint32_t e_cur[8], e_nxt[8], l_cur[8], l_nxt[8];
   if (has_ein) load_row16_raw(J.ein, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, e_cur);
@@ -316,8 +318,8 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
       } else if (EPI == EPI_POLY) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          o[2 * i] = fmaf(P.cc, __uint_as_float(acc[2 * i]), P.cb * bf16_lo(e_cur[i]));
-          o[2 * i + 1] = fmaf(P.cc, __uint_as_float(acc[2 * i + 1]), P.cb * bf16_hi(e_cur[i]));
+          o[2 * i] = fmaf(cc, __uint_as_float(acc[2 * i]), cb * bf16_lo(e_cur[i]));
+          o[2 * i + 1] = fmaf(cc, __uint_as_float(acc[2 * i + 1]), cb * bf16_hi(e_cur[i]));
         }
       } else {
 #pragma unroll
@@ -327,8 +329,8 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
             x0 += bf16_lo(l_cur[i]);
             x1 += bf16_hi(l_cur[i]);
           }
-          o[2 * i] = J.alpha * fmaf(P.ca, x0, __uint_as_float(acc[2 * i]));
-          o[2 * i + 1] = J.alpha * fmaf(P.ca, x1, __uint_as_float(acc[2 * i + 1]));
+          o[2 * i] = J.alpha * fmaf(ca, x0, __uint_as_float(acc[2 * i]));
+          o[2 * i + 1] = J.alpha * fmaf(ca, x1, __uint_as_float(acc[2 * i + 1]));
         }
       }
       uint32_t pk[8];
@@ -616,6 +618,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       if (tk.ph == EPI_APPLY && tk.it > 0) ld_acquire(done_counter(B, tk.mat, tk.it - 1, EPI_APPLY));
       EpiJob J;
       J.mat = tk.mat;
+      J.it = tk.it;
       J.m0 = tk.m0;
       J.n0 = tk.n0;
       J.nt = tk.nt;

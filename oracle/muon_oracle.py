@@ -112,19 +112,30 @@ def frobenius_scale(u: np.ndarray) -> float:
     return 1.0 / (math.sqrt(float(np.sum(np.square(np.asarray(u, _F64))))) + NS_EPS)
 
 
+def step_coeffs(steps: int, coeffs) -> list:
+    """(a, b, c) of each of `steps` steps: one triple for every step, or one triple per step
+    (a schedule of per-iteration coefficients)."""
+    c = np.asarray(coeffs, dtype=_F64)
+    if c.shape == (3,):
+        return [tuple(c)] * steps
+    if c.shape != (steps, 3):
+        raise ValueError(f"coefficients must be one (a, b, c) or one per step, got shape {c.shape}")
+    return [tuple(r) for r in c]
+
+
 def newton_schulz(u: np.ndarray, steps: int = NS_STEPS, coeffs=(NS_A, NS_B, NS_C)) -> np.ndarray:
     """Quintic Newton-Schulz orthogonalisation of one matrix, in fp64.
 
     X0 = u / (||u||_F + eps); a tall matrix iterates on its transpose so that
-    A is min(r, c) square; each step forms A = X X^T, B = b A + c A A and
-    X <- a X + B X; the result is returned in the input's orientation.
+    A is min(r, c) square; step i forms A = X X^T, B = b_i A + c_i A A and
+    X <- a_i X + B X; the result is returned in the input's orientation.
+    `coeffs` is one (a, b, c) for every step, or one per step.
     """
-    a, b, c = coeffs
     x = np.asarray(u, dtype=_F64) * frobenius_scale(u)
     tall = x.shape[0] > x.shape[1]
     if tall:
         x = x.T
-    for _ in range(steps):
+    for a, b, c in step_coeffs(steps, coeffs):
         A = x @ x.T
         B = b * A + c * (A @ A)
         x = a * x + B @ x
@@ -132,10 +143,9 @@ def newton_schulz(u: np.ndarray, steps: int = NS_STEPS, coeffs=(NS_A, NS_B, NS_C
 
 
 def quintic(x, steps: int = NS_STEPS, coeffs=(NS_A, NS_B, NS_C)):
-    """The scalar map p(x) = a x + b x^3 + c x^5 composed `steps` times."""
-    a, b, c = coeffs
+    """The scalar maps p_i(x) = a_i x + b_i x^3 + c_i x^5 composed over `steps` steps."""
     x = np.asarray(x, dtype=_F64)
-    for _ in range(steps):
+    for a, b, c in step_coeffs(steps, coeffs):
         x = a * x + b * x ** 3 + c * x ** 5
     return x
 

@@ -139,6 +139,13 @@ def test_stage_argument_errors(lib):
     sh = b.shape_of(1, 8, 8)
     assert lib.mb_momentum(None, good, good, sh, 0.9, None) == b.MB_ERR_NULL
     assert lib.mb_newton_schulz(good, good, sh, 99, good, 1 << 20, None) == b.MB_ERR_NS_STEPS
+    abc = (ctypes.c_float * 6)(3.4445, -4.775, 2.0315, 1.875, -1.25, 0.375)
+    assert lib.mb_newton_schulz_coeffs(good, good, sh, 2, None, good, 1 << 20, None) == b.MB_ERR_NULL
+    assert lib.mb_newton_schulz_coeffs(good, good, sh, 17, abc, good, 1 << 20, None) == b.MB_ERR_NS_STEPS
+    abc[4] = float("nan")
+    assert lib.mb_newton_schulz_coeffs(good, good, sh, 2, abc, good, 1 << 20, None) == b.MB_ERR_ARG
+    abc[4] = -1.25
+    assert lib.mb_newton_schulz_coeffs(good, good, b.shape_of(0, 8, 8), 2, abc, good, 1 << 20, None) == b.MB_ERR_SHAPE
     assert lib.mb_update(good, good, None, sh, 0.02, 0.01, None) == b.MB_ERR_NULL
     assert lib.mb_normuon_update(good, good, good, good, sh, 0.02, 0.01, 0.95, good, 8, None) == b.MB_ERR_WORKSPACE
 

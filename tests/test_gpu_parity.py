@@ -122,6 +122,32 @@ def test_newton_schulz_steps(nss, steps, shape):
     assert errs.max() <= ns_tol(*shape[1:], steps=steps), errs
 
 
+# a schedule of per-step coefficients: the pages' quintic, then the classical (15/8, -10/8, 3/8)
+SCHEDULE = [(3.4445, -4.7750, 2.0315)] * 3 + [(1.875, -1.25, 0.375)] * 2
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 384), (2, 384, 256), (2, 12, 40), (1, 768, 3072)])
+def test_newton_schulz_coefficient_schedule(nss, shape):
+    rng = np.random.default_rng(sum(shape) + 1)
+    u = synth.to_bf16_bits(rng.standard_normal(shape))
+    ut = to_dev(u)
+    vt = torch.empty_like(ut)
+    nss.mb_newton_schulz_coeffs(ut, vt, SCHEDULE)
+    torch.cuda.synchronize()
+    assert nss.mb_sync_status() == 0
+    v = u16(vt)
+    errs = np.array([O.rel_frobenius(O.bf16_bits_to_f64(v[k]),
+                                     O.newton_schulz(O.bf16_bits_to_f64(u[k]), 5, SCHEDULE)) for k in range(shape[0])])
+    assert errs.max() <= ns_tol(*shape[1:]), errs
+    # the pages' quintic written out for every step is the plain call, bit for bit
+    wt = torch.empty_like(ut)
+    nss.mb_newton_schulz_coeffs(ut, wt, [(3.4445, -4.7750, 2.0315)] * 5)
+    xt = torch.empty_like(ut)
+    nss.mb_newton_schulz(ut, xt, ns_steps=5)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(wt), u16(xt))
+
+
 def test_newton_schulz_zero_and_scaled_input(nss):
     shape = (4, 256, 256)
     u = synth.to_bf16_bits(np.random.default_rng(3).standard_normal(shape))

@@ -138,6 +138,36 @@ def test_ns_spectral_closed_form(rows, cols):
     assert O.rel_frobenius(got, expect) < 1e-12
 
 
+def test_ns_per_step_coefficients_closed_form():
+    """A schedule of per-step (a, b, c): NS(G) = U diag(p_5 o ... o p_1(s / (||s||_2 + eps))) V^T,
+    the matrix iteration against the scalar maps on the singular values."""
+    rng = np.random.default_rng(77)
+    sched = [(O.NS_A, O.NS_B, O.NS_C)] * 3 + [(1.875, -1.25, 0.375)] * 2
+    for rows, cols in [(12, 20), (20, 12)]:
+        k = min(rows, cols)
+        U, V = _orth(rng, rows, k), _orth(rng, cols, k)
+        s = np.exp(rng.uniform(-4, 0, k))
+        G = (U * s) @ V.T
+        expect = (U * O.quintic(s / (np.linalg.norm(s) + O.NS_EPS), steps=5, coeffs=sched)) @ V.T
+        assert O.rel_frobenius(O.newton_schulz(G, steps=5, coeffs=sched), expect) < 1e-12
+    # one triple for every step is the same schedule written out
+    G = rng.standard_normal((9, 14))
+    assert np.array_equal(O.newton_schulz(G, 4, [(O.NS_A, O.NS_B, O.NS_C)] * 4), O.newton_schulz(G, 4))
+    with pytest.raises(ValueError):
+        O.newton_schulz(G, 5, sched[:4])
+
+
+def test_ns_classical_quintic_reaches_the_polar_factor():
+    """The classical quintic (15/8, -10/8, 3/8) has p(1) = 1 and p'(1) = 0: iterated long enough
+    from a well-conditioned matrix it reaches the polar factor U V^T of the SVD."""
+    rng = np.random.default_rng(5)
+    for shape in [(12, 8), (8, 12)]:
+        G = rng.standard_normal(shape)
+        Uf, _, Vt = np.linalg.svd(G, full_matrices=False)
+        got = O.newton_schulz(G, steps=40, coeffs=(1.875, -1.25, 0.375))
+        assert O.rel_frobenius(got, Uf @ Vt) < 1e-10
+
+
 def test_ns_svd_brute_force_small():
     """U^T NS(G) V is diagonal and holds the scalar map of the normalised singular values."""
     rng = np.random.default_rng(5)
