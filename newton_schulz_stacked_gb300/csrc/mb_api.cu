@@ -336,6 +336,9 @@ void set_coeffs(float* ca, float* cb, float* cc, int steps, const float* coeffs)
   }
 }
 
+int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds, const float* coeffs,
+                      SideStream* side, int n_small);
+
 // S3-S4 for every bank: the result lands in x[final_buffer(steps)].
 int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds,
              const float* coeffs = nullptr) {
@@ -358,6 +361,20 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds,
     MB_TRY_CUDA(cudaEventRecord(side->fork, st));
     MB_TRY_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
   }
+  const int r = stage_ns_launches(b, nb, steps, st, ds, coeffs, side, n_small);
+  // the caller's stream waits for the side stream on every path, so that nothing launched
+  // there outlives the call in stream order, even when a later launch failed
+  if (side) {
+    const cudaError_t e1 = cudaEventRecord(side->join, side->stream);
+    const cudaError_t e2 = e1 == cudaSuccess ? cudaStreamWaitEvent(st, side->join, 0) : e1;
+    if (r == MB_OK && e2 != cudaSuccess) return cuda_fail(e2);
+  }
+  return r;
+}
+
+// The launches of stage_ns after the fork of the side stream (null when unused).
+int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds, const float* coeffs,
+                      SideStream* side, int n_small) {
   // small matrices: fp32 SIMT path; one launch for those whose iteration fits in
   // shared memory, one for the rest
   for (int pass = 0; pass < 2 && n_small > 0; ++pass) {
@@ -392,7 +409,6 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds,
       MB_LAUNCH(launch_small_ns(sp, in_smem, st), sp.total_blocks > 0, MB_MARK_SMALL_NS, st);
     }
   }
-  if (side) MB_TRY_CUDA(cudaEventRecord(side->join, side->stream));
   // large matrices: every step of every bank in one fused tcgen05 launch (up to MAX_NS_BANKS banks each)
   int large[MAX_BANKS], nl = 0;
   for (int i = 0; i < nb; ++i)
@@ -471,7 +487,6 @@ int stage_ns(const Bank* b, int nb, int steps, cudaStream_t st, DeviceState* ds,
     np.next_task = reinterpret_cast<unsigned*>(first.ws + first.L.sync + first.L.sync_bytes - 16);
     MB_LAUNCH(launch_ns_fused(np, st), np.total_tasks > 0, MB_MARK_NS_GEMM, st);
   }
-  if (side) MB_TRY_CUDA(cudaStreamWaitEvent(st, side->join, 0));
   return MB_OK;
 }
 
