@@ -73,7 +73,8 @@ enum {
   MB_ERR_ARG = -8,           /* a scalar argument is not finite, or beta2/mu outside [0, 1] */
   MB_ERR_UNSUPPORTED = -9,   /* the current device is not sm_103 */
   MB_ERR_TOO_MANY = -10,     /* more banks than one call accepts */
-  MB_ERR_SCRATCH_LIMIT = -11 /* mb_newton_schulz_noalloc: the shape needs more than its fixed scratch */
+  MB_ERR_SCRATCH_LIMIT = -11, /* mb_newton_schulz_noalloc: the shape needs more than its fixed scratch */
+  MB_ERR_DEVICE = -12        /* a device-side consistency check failed (from mb_sync_status) */
 };
 
 /* One bank: `batch` matrices of rows x cols. */
@@ -205,8 +206,8 @@ int mb_workspace_views(mb_shape shape, int normuon, int ns_steps, size_t* u_offs
                        size_t* v_offset, size_t* row_pitch);
 
 /* Synchronises `cuda_stream`, then returns and clears this device's latched
- * device-side status (MB_OK, MB_ERR_TIMEOUT, or MB_ERR_ARG for a bad scalar
- * read by muon_multi_step_dev), or MB_ERR_CUDA. */
+ * device-side status (MB_OK, MB_ERR_TIMEOUT, MB_ERR_ARG for a bad scalar read
+ * by muon_multi_step_dev, or MB_ERR_DEVICE), or MB_ERR_CUDA. */
 int mb_sync_status(void* cuda_stream);
 
 /* Runs the bounded-wait primitive of the kernels against an mbarrier that

@@ -27,6 +27,7 @@ MB_ERR_ARG = -8
 MB_ERR_UNSUPPORTED = -9
 MB_ERR_TOO_MANY = -10
 MB_ERR_SCRATCH_LIMIT = -11
+MB_ERR_DEVICE = -12
 MB_NOALLOC_SCRATCH_BYTES = 32 << 20
 MB_MAX_BANKS = 8
 

@@ -433,17 +433,13 @@ int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceS
       NsBank& nb_ = np.bank[j];
       for (int t = 0; t < 3; ++t) {
         MB_TRY(encode_map(&nb_.xk[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 128));
-        MB_TRY(encode_map(&nb_.xk2[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 64, 256));
         MB_TRY(encode_mn_map(&nb_.xmn2[t], k.ws + L.x[t], L.rows, L.batch, L.ld, 2));
-        MB_TRY(encode_mn_map(&nb_.xmn4[t], k.ws + L.x[t], L.rows, L.batch, L.ld, 4));
         MB_TRY(encode_map(&nb_.st_x[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 32, 32,
                           CU_TENSOR_MAP_SWIZZLE_64B));
         nb_.x[t] = k.at<uint16_t>(L.x[t]);
       }
       MB_TRY(encode_map(&nb_.ak, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 128));
-      MB_TRY(encode_map(&nb_.ak2, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 256));
       MB_TRY(encode_map(&nb_.bk, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 128));
-      MB_TRY(encode_map(&nb_.bk2, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 256));
       MB_TRY(encode_map(&nb_.st_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       MB_TRY(encode_map(&nb_.st_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       nb_.a = k.at<uint16_t>(L.a);
@@ -459,13 +455,13 @@ int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceS
       nb_.m = L.m;
       nb_.n = L.n;
       nb_.tall = L.tall;
+      // pair tasks: 256 x 256 tiles of A and B on or above the diagonal, 256 x 256 tiles of X'
       nb_.T = (L.m + 127) / 128;
-      int t = 0;
-      for (int I = 0; I < nb_.T; ++I) t += (nb_.T - I + 1) / 2;
-      nb_.sym_tiles = t;
+      const int P2 = (nb_.T + 1) / 2;
+      nb_.sym_pairs = P2 * (P2 + 1) / 2;
       const int M = L.tall ? L.n : L.m, N = L.tall ? L.m : L.n;
       nb_.tn = (N + 255) / 256;
-      nb_.apply_tiles = ((M + 127) / 128) * nb_.tn;
+      nb_.apply_pairs = ((M + 255) / 256) * nb_.tn;
       MB_TRY_CUDA(cudaMemsetAsync(k.ws + L.sync, 0, L.sync_bytes, st));
     }
     // task numbering inside one step: phase, then bank, then matrix and tile
@@ -477,7 +473,7 @@ int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceS
         np.seg_bank[np.nseg] = static_cast<unsigned char>(j);
         np.seg_ph[np.nseg] = static_cast<unsigned char>(ph);
         ++np.nseg;
-        per_iter += np.bank[j].batch * (ph == EPI_APPLY ? np.bank[j].apply_tiles : np.bank[j].sym_tiles);
+        per_iter += np.bank[j].batch * (ph == EPI_APPLY ? np.bank[j].apply_pairs : np.bank[j].sym_pairs);
       }
     }
     np.seg_begin[np.nseg] = per_iter;
@@ -679,6 +675,7 @@ const char* mb_status_string(int status) {
     case MB_ERR_UNSUPPORTED: return "device is not sm_103";
     case MB_ERR_TOO_MANY: return "too many banks in one call";
     case MB_ERR_SCRATCH_LIMIT: return "shape needs more than the fixed no-alloc scratch (MB_NOALLOC_SCRATCH_BYTES)";
+    case MB_ERR_DEVICE: return "device-side consistency check failed";
     default: return "unknown status";
   }
 }
@@ -838,7 +835,7 @@ int mb_sync_status(void* cuda_stream) {
   MB_TRY_CUDA(cudaMemcpy(&h, ds->status, sizeof(int), cudaMemcpyDeviceToHost));
   const int zero = 0;
   MB_TRY_CUDA(cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice));
-  return h == DEV_OK ? MB_OK : h == DEV_BAD_SCALAR ? MB_ERR_ARG : MB_ERR_TIMEOUT;
+  return h == DEV_OK ? MB_OK : h == DEV_TIMEOUT ? MB_ERR_TIMEOUT : h == DEV_BAD_SCALAR ? MB_ERR_ARG : MB_ERR_DEVICE;
 }
 
 int mb_selftest_timeout(unsigned limit_us, void* cuda_stream) {

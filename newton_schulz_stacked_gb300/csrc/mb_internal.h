@@ -111,13 +111,13 @@ constexpr int MAX_NS_BANKS = 4;     // large banks per fused Newton-Schulz launc
 // One large bank in the fused Newton-Schulz launch.  x[0] holds u; the
 // iterates X_1, X_2, ... alternate between x[1] and x[2].
 // Every operand tile of one 64-deep k-block is a single TMA box: K-major boxes
-// of 128 or 256 rows, and MN-major boxes of 2 or 4 chunks of 64 columns through
-// a 4-D view {64 columns, rows, row pitch / 64 chunks, matrix} of an X buffer
-// (large banks pitch their X buffers to a multiple of 64 columns for it).
+// of 128 rows, and MN-major boxes of 2 chunks of 64 columns through a 4-D view
+// {64 columns, rows, row pitch / 64 chunks, matrix} of an X buffer (large banks
+// pitch their X buffers to a multiple of 64 columns for it).
 struct NsBank {
-  CUtensorMap xk[3], xk2[3];        // X buffers, K-major boxes of 128 and 256 rows x 64
-  CUtensorMap xmn2[3], xmn4[3];     // X buffers, MN-major boxes of 64 K rows x 128 and 256 columns
-  CUtensorMap ak, ak2, bk, bk2;     // A and B, K-major boxes of 128 and 256 rows x 64
+  CUtensorMap xk[3];                // X buffers, K-major boxes of 128 rows x 64
+  CUtensorMap xmn2[3];              // X buffers, MN-major boxes of 64 K rows x 128 columns
+  CUtensorMap ak, bk;               // A and B, K-major boxes of 128 rows x 64
   CUtensorMap st_x[3], st_a, st_b;  // 32x32 store boxes (64-byte swizzle)
   const uint16_t* x[3];             // X buffers (APPLY's epilogue input)
   const uint16_t* a;                // A (POLY's epilogue input)
@@ -125,8 +125,8 @@ struct NsBank {
   const float* scale;               // per-matrix 1/(||u||_F + eps)
   unsigned* done;                   // completion counters [batch][MAX_NS_STEPS][3], zeroed before launch
   int batch, rows, cols, m, n, tall;
-  int T, sym_tiles;                 // 128-blocks per side of A; tiles per matrix of GRAM and POLY
-  int tn, apply_tiles;              // 256-wide column tiles and tiles per matrix of APPLY
+  int T, sym_pairs;                 // 128-blocks per side of A; pair tasks per matrix of GRAM and POLY
+  int tn, apply_pairs;              // 256-wide column tiles and pair tasks per matrix of APPLY
 };
 
 struct NsParams {

@@ -10,35 +10,52 @@
 // swapped-operand form A = X^T X, X' = beta (a X + X B); the difference is
 // only which operand tiles are K-major and which are MN-major.
 //
-// A and B are symmetric: GRAM and POLY compute only the 128x128 blocks on or
-// above the diagonal (paired into 128x256 tiles) and store each off-diagonal
-// block twice, directly and mirrored, so the next phase reads a full matrix.
+// CTA pairs.  The kernel runs in clusters of two CTAs (one per SM) that compute
+// one 256 x nt output tile (nt = 128 or 256) with M = 256 tcgen05 MMAs
+// (cta_group::2): CTA r holds tile rows 128r .. 128r+127 of the A operand and
+// half of the B operand's nt rows, and its TMEM receives its 128 rows x all nt
+// columns.  Each SM therefore stages 32 KB of operands per 64-deep k-block
+// instead of 48 KB for a 128 x 256 tile alone: a third less L2-to-SM traffic,
+// and six stages in flight where four fitted before.
 //
-// Scheduling.  The work of all steps is one list of tasks (an output tile of
-// one phase of one matrix), ordered by step, then by (bank, phase) segment in
-// the order the host gives (any order that puts each bank's GRAM before its
-// POLY before its APPLY), then matrix and tile.  Persistent CTAs, one per SM, claim tasks in that order from a
-// global counter.  A task's producer first waits until every tile of the
-// previous phase of the same matrix has been stored (per-matrix completion
-// counters, release/acquire at GPU scope), so phases overlap across matrices
-// and there is no launch boundary between them.  Every task depends only on
-// earlier tasks and all CTAs are resident, so the earliest unfinished task
-// can always run; each wait is bounded all the same.
+// A and B are symmetric: GRAM and POLY compute only the 256 x 256 tiles (2 x 2
+// aligned 128-blocks) that touch the upper triangle.  Each block above the
+// diagonal is stored twice, directly and mirrored, so the next phase reads a
+// full matrix; a block on the diagonal is made symmetric before its store, and
+// the one block below the diagonal of a diagonal tile is computed but not stored.
 //
-// CTA roles (11 warps):
-//   warp 10 lane 0: scheduler: claims the next task, decodes it and waits until
-//                   its inputs are stored, one task ahead of the producer, and
-//                   hands the decoded task to the other roles through a ring of
-//                   task records in shared memory
-//   warp 0 lane 0 : TMA producer of a STAGES-deep ring of (A 128x64, B 256x64)
-//                   bf16 tiles, one TMA box per operand and k-block (a producer
-//                   thread pays about as much per TMA instruction as an MMA of
-//                   one 16-deep slice takes, so each operand is a single box)
-//   warp 1        : owns 512 TMEM columns = two 256-column fp32 accumulators;
-//                   lane 0 issues tcgen05.mma (K = 16 per instruction)
-//   warps 2..9    : epilogue, two warps per 32-lane TMEM quadrant (each takes
-//                   half the columns); task k's epilogue runs under task k+1's
-//                   MMAs; results leave through shared memory by TMA bulk stores
+// Scheduling.  The work of all steps is one list of pair tasks (a 256-row
+// output tile of one phase of one matrix), ordered by step, then by (bank,
+// phase) segment in the order the host gives (any order that puts each bank's
+// GRAM before its POLY before its APPLY), then matrix and tile.  The even CTA
+// of each pair claims tasks from a global counter and hands them to both CTAs.
+// A task's loads first wait until every tile of the previous phase of the same
+// matrix has been stored (per-matrix completion counters, release/acquire at
+// GPU scope), so phases overlap across matrices and there is no launch
+// boundary between them.  Every task depends only on earlier tasks and all
+// pairs are resident, so the earliest unfinished task can always run; each
+// wait is bounded all the same.
+//
+// CTA roles (11 warps, both CTAs unless noted):
+//   warp 10 lane 0: (even CTA) scheduler: claims the next task, decodes it and
+//                   waits until its inputs are stored, one task ahead of the
+//                   producer, and writes the decoded task into both CTAs' ring
+//                   of task records (the odd CTA's through distributed shared
+//                   memory); (odd CTA) relay: once every reader of a record in
+//                   the odd CTA has taken it, tells the scheduler with one
+//                   cluster-scope arrival
+//   warp 0 lane 0 : TMA producer of a STAGES-deep ring of (A 128x64, B-half
+//                   128x64) bf16 tiles, one TMA box per operand and k-block (a
+//                   producer thread pays about as much per TMA instruction as an
+//                   MMA of one 16-deep slice takes); the bytes of both CTAs
+//                   complete on the even CTA's stage barrier
+//   warp 1        : allocates 512 TMEM columns in both CTAs = two 256-column
+//                   fp32 accumulators; (even CTA) lane 0 issues the MMAs and
+//                   releases each stage in both CTAs with a multicast commit
+//   warps 2..9    : epilogue of the CTA's own 128 rows, two warps per 32-lane
+//                   TMEM quadrant (each takes half the columns); task k's
+//                   epilogue runs under task k+1's MMAs; results leave through
+//                   shared memory by TMA bulk stores
 #include <atomic>
 
 #include "mb_device.cuh"
@@ -48,29 +65,36 @@ namespace mb {
 
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                      // rows of a tile per CTA
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_TILE_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_TILE_BYTES = 256 * BK * 2;  // 32 KB
-constexpr int TILE_SMEM = STAGES * (A_TILE_BYTES + B_TILE_BYTES);
+constexpr int STAGES = 6;
+constexpr int A_TILE_BYTES = BM * BK * 2;    // 16 KB
+constexpr int BH_TILE_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of a 256-row B operand
+constexpr int STAGE_BYTES = A_TILE_BYTES + BH_TILE_BYTES;
+constexpr int TILE_SMEM = STAGES * STAGE_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_BUF_BYTES = 4096;          // per epilogue warp: 32x32 bf16 chunk + its transpose
 constexpr int EPI_SMEM = EPI_WARPS * EPI_BUF_BYTES;
-constexpr int TASK_SLOTS = 4;                // claimed tasks in flight inside a CTA
+constexpr int TASK_SLOTS = 4;                // claimed tasks in flight inside a pair
+// threads that read a task record and arrive on their own CTA's slot_empty barrier: in the
+// even CTA its producer, the MMA issuer, its epilogue warps and the odd CTA's relay; in the
+// odd CTA its producer and epilogue warps
+constexpr int SLOT_READERS_EVEN = 1 + 1 + EPI_WARPS + 1;
+constexpr int SLOT_READERS_ODD = 1 + EPI_WARPS;
 constexpr int GEMM_SMEM = TILE_SMEM + EPI_SMEM + 1024 /* alignment slack */ + 512 /* barriers, slots */;
 constexpr int SCHED_WARP = 2 + EPI_WARPS;
 constexpr int GEMM_THREADS = 32 * (3 + EPI_WARPS);
-constexpr uint32_t ACC_COLS = 256;          // one accumulator
+constexpr uint32_t ACC_COLS = 256;           // one accumulator
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
 // ---------------------------------------------------------------- tasks
 
-// One task, as the scheduler hands it over (t < 0: no more tasks).
+// One pair task, as the scheduler hands it over (t < 0: no more tasks).  The
+// CTA of pair rank r computes rows m0 + 128 r .. m0 + 128 r + 127.
 struct Task {
   int t;                 // task index
   int it, ph, bi, mat;   // step, phase, bank, matrix
-  int m0, n0, nt;        // output tile origin and width (128 or 256)
+  int m0, n0, nt;        // output tile origin (of the pair) and width (128 or 256)
 };
 
 __device__ __forceinline__ int iterate_buffer(int k) { return k == 0 ? 0 : 1 + ((k - 1) & 1); }
@@ -88,40 +112,44 @@ __device__ __forceinline__ void decode_task(const NsParams& P, int t, Task& k) {
   k.m0 = k.n0 = 0;
   k.nt = 128;
   if (k.ph != EPI_APPLY) {
-    k.mat = r / B.sym_tiles;
-    r -= k.mat * B.sym_tiles;
-    for (int I = 0; I < B.T; ++I) {
-      const int c = (B.T - I + 1) >> 1;
+    // block-row pair q (128-blocks 2q, 2q+1) takes the block-column pairs p = q .. P2-1
+    k.mat = r / B.sym_pairs;
+    r -= k.mat * B.sym_pairs;
+    const int P2 = (B.T + 1) >> 1;
+    for (int q = 0; q < P2; ++q) {
+      const int c = P2 - q;
       if (r < c) {
-        const int J = I + 2 * r;
-        k.m0 = I * BM;
-        k.n0 = J * BM;
-        k.nt = (J + 1 < B.T) ? 256 : 128;
+        const int p = q + r;
+        k.m0 = 2 * q * BM;
+        k.n0 = 2 * p * BM;
+        k.nt = (2 * p + 1 < B.T) ? 256 : 128;
         return;
       }
       r -= c;
     }
   } else {
-    k.mat = r / B.apply_tiles;
-    r -= k.mat * B.apply_tiles;
-    const int tm = r / B.tn, tj = r - tm * B.tn;
+    k.mat = r / B.apply_pairs;
+    r -= k.mat * B.apply_pairs;
+    const int tm2 = r / B.tn, tj = r - tm2 * B.tn;
     const int N = B.tall ? B.m : B.n;
-    k.m0 = tm * BM;
+    k.m0 = 2 * tm2 * BM;
     k.n0 = tj * 256;
     k.nt = (N - k.n0 > 128) ? 256 : 128;
   }
 }
 
+// Tiles (one per CTA of a pair task) per matrix of a phase: what its completion counter reaches.
 __device__ __forceinline__ int phase_tiles(const NsBank& B, int ph) {
-  return ph == EPI_APPLY ? B.apply_tiles : B.sym_tiles;
+  return 2 * (ph == EPI_APPLY ? B.apply_pairs : B.sym_pairs);
 }
 
 __device__ __forceinline__ unsigned* done_counter(const NsBank& B, int mat, int it, int ph) {
   return B.done + (static_cast<size_t>(mat) * MAX_NS_STEPS + it) * 3 + ph;
 }
 
-// Operands of a task's GEMM: the map of each operand's single box per k-block
-// (A: 128 rows or 128 MN columns; B: nt rows or nt MN columns).
+// Operands of a task's GEMM in one CTA of the pair: each is one box per k-block
+// of 128 rows (K-major) or 128 columns (MN-major).  A CTA's half of a 128-wide B
+// operand is 64 rows or columns; its box then also carries 64 that are not read.
 struct Operands {
   const CUtensorMap* a;
   const CUtensorMap* b;
@@ -130,32 +158,24 @@ struct Operands {
 
 __device__ __forceinline__ Operands task_operands(const NsBank& B, const Task& k) {
   const int cur = iterate_buffer(k.it);
-  const bool wide = k.nt > 128;
   Operands o;
   if (k.ph == EPI_GRAM) {
-    if (B.tall) {        // A = X^T X: columns of X on both sides
-      o.a = &B.xmn2[cur];
-      o.b = wide ? &B.xmn4[cur] : &B.xmn2[cur];
-    } else {             // A = X X^T: rows of X on both sides
-      o.a = &B.xk[cur];
-      o.b = wide ? &B.xk2[cur] : &B.xk[cur];
-    }
+    o.a = o.b = B.tall ? &B.xmn2[cur] : &B.xk[cur];   // A = X^T X (columns of X) or X X^T (rows)
     o.a_mn = o.b_mn = B.tall;
     o.K = B.n;
   } else if (k.ph == EPI_POLY) {
-    o.a = &B.ak;
-    o.b = wide ? &B.ak2 : &B.ak;
+    o.a = o.b = &B.ak;
     o.a_mn = o.b_mn = 0;
     o.K = B.m;
   } else {
     if (!B.tall) {       // X' = a X + B X: rows of B (K-major), X as MN-major tiles
       o.a = &B.bk;
-      o.b = wide ? &B.xmn4[cur] : &B.xmn2[cur];
+      o.b = &B.xmn2[cur];
       o.a_mn = 0;
       o.b_mn = 1;
     } else {             // X' = a X + X B: rows of X and of B, both K-major
       o.a = &B.xk[cur];
-      o.b = wide ? &B.bk2 : &B.bk;
+      o.b = &B.bk;
       o.a_mn = 0;
       o.b_mn = 0;
     }
@@ -258,9 +278,10 @@ constexpr int LO_WRITE = 1, LO_READ = 2;
 // 16 columns at a time with the next 16 columns' input prefetched.
 // Each 32x32 chunk is staged in the warp's shared buffer and written with a
 // TMA bulk store; a symmetric phase also stores the transposed chunk at the
-// mirrored position.  In a diagonal 128-block the chunks below the diagonal
-// are not stored (their mirror covers them) and the chunk on the diagonal is
-// made symmetric before its store, so every element is written exactly once.
+// mirrored position.  A 128-block below the diagonal is not stored at all; in
+// a diagonal 128-block the chunks below the diagonal are not stored (their
+// mirror covers them) and the chunk on the diagonal is made symmetric before
+// its store, so every element is written exactly once.
 template <int EPI, int LO>
 __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uint32_t tacc, int quad, int half,
                                          int lane, uint8_t* ebuf) {
@@ -289,7 +310,9 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
     bool direct = row0 < J.M && col0 < J.N, mirror = false, diag = false;
     if (J.sym) {
       const int Jb = col0 / BM;
-      if (Jb != I) {
+      if (Jb < I) {
+        direct = false;                         // below the diagonal: block (Jb, I) is stored mirrored
+      } else if (Jb > I) {
         mirror = direct;
       } else {
         const int cq = (col0 % BM) / 32;
@@ -407,19 +430,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_TILE_BYTES;
   uint8_t* sEpi = smem + TILE_SMEM;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TILE_SMEM + EPI_SMEM);
-  uint64_t* empty = full + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TILE_SMEM + EPI_SMEM);  // [STAGES] (even) both halves landed
+  uint64_t* empty = full + STAGES;                // [STAGES] the pair's MMAs are done with the stage
   uint64_t* tfull = empty + STAGES;               // [2] accumulator ready for the epilogue
-  uint64_t* tempty = tfull + 2;                   // [2] accumulator drained by the epilogue
+  uint64_t* tempty = tfull + 2;                   // [2] (even) both CTAs' epilogues drained the accumulator
   uint64_t* slot_full = tempty + 2;               // [TASK_SLOTS] task record written
-  uint64_t* slot_empty = slot_full + TASK_SLOTS;  // [TASK_SLOTS] producer, MMA and epilogue warps have read it
-  uint64_t* prod_took = slot_empty + TASK_SLOTS;  // [TASK_SLOTS] the producer has started the task
+  uint64_t* slot_empty = slot_full + TASK_SLOTS;  // [TASK_SLOTS] (even) every reader of both CTAs has it
+  uint64_t* prod_took = slot_empty + TASK_SLOTS;  // [TASK_SLOTS] (even) the even producer has started the task
   uint64_t* tile_done = prod_took + TASK_SLOTS;   // every epilogue warp's stores of a task are complete
   Task* rec = reinterpret_cast<Task*>(tile_done + 2);   // [TASK_SLOTS] (16-byte aligned)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rec + TASK_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -428,11 +453,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], EPI_WARPS);
+      mbar_init(&tempty[b], 2 * EPI_WARPS);
     }
     for (int s = 0; s < TASK_SLOTS; ++s) {
       mbar_init(&slot_full[s], 1);
-      mbar_init(&slot_empty[s], EPI_WARPS + 2);
+      mbar_init(&slot_empty[s], even ? SLOT_READERS_EVEN : SLOT_READERS_ODD);
       mbar_init(&prod_took[s], 1);
     }
     mbar_init(tile_done, EPI_WARPS);
@@ -440,11 +465,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
     mbar_init_fence();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();      // both CTAs' barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -452,13 +478,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
     latch_status(P.status, DEV_TIMEOUT);
     *abort_flag = 1;
   };
+  // The pair's MMAs write the odd CTA's accumulators at the even CTA's TMEM address.
+  if (threadIdx.x == 0 && ld_cluster_u32(map_to_rank(tmem_slot, rank ^ 1u)) != tmem) {
+    latch_status(P.status, DEV_PAIR_TMEM);
+    *abort_flag = 1;
+  }
+  // A reader of record s reports that it has the task (the odd CTA's relay forwards its
+  // CTA's reports to the even CTA's scheduler).
+  auto release_slot = [&](int s) { mbar_arrive(&slot_empty[s]); };
+  // Every role reads the next pair task from record k % TASK_SLOTS (t < 0 ends the loop).
+  auto read_slot = [&](uint32_t k, Task& tk) -> bool {
+    const int s = k % TASK_SLOTS;
+    if (!mbar_wait_cluster_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
+      fail();
+      return false;
+    }
+    tk = rec[s];
+    return true;
+  };
 
   if (warp == SCHED_WARP) {
-    if (lane == 0) {
+    if (even && lane == 0) {
       // ---------------- scheduler: claim, decode, wait for the inputs; at most one task ahead of the producer
+      const uint32_t rec_odd = map_to_rank(rec, 1);
       for (uint32_t k = 0;; ++k) {
         const int s = k % TASK_SLOTS;
-        if (k >= TASK_SLOTS && !mbar_wait_or_abort(&slot_empty[s], ((k / TASK_SLOTS) - 1) & 1, abort_flag)) {
+        if (k >= TASK_SLOTS &&
+            !mbar_wait_cluster_or_abort(&slot_empty[s], ((k / TASK_SLOTS) - 1) & 1, abort_flag)) {
           fail();
           break;
         }
@@ -486,53 +532,71 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
           }
         }
         rec[s] = tk;
+        const uint4* w = reinterpret_cast<const uint4*>(&tk);
+        st_cluster_v4(rec_odd + s * sizeof(Task), w[0]);
+        st_cluster_v4(rec_odd + s * sizeof(Task) + 16, w[1]);
         mbar_arrive(&slot_full[s]);
+        mbar_arrive_cluster(map_to_rank(&slot_full[s], 1));
         if (tk.t < 0) break;
+      }
+    } else if (!even && lane == 0) {
+      // ---------------- relay: once every reader of record k in this CTA has it, one
+      // cluster-scope arrival tells the scheduler that the record may be overwritten
+      const uint32_t slot_empty_even = map_to_rank(&slot_empty[0], 0);
+      for (uint32_t k = 0;; ++k) {
+        const int s = k % TASK_SLOTS;
+        if (!mbar_wait_cluster_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        const bool last = rec[s].t < 0;
+        if (!mbar_wait_or_abort(&slot_empty[s], (k / TASK_SLOTS) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        mbar_arrive_cluster(slot_empty_even + 8u * static_cast<uint32_t>(s));
+        if (last) break;
       }
     }
   } else if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs)
       for (int b = 0; b < P.nbank; ++b) {
         tma_prefetch_map(&P.bank[b].ak);
-        tma_prefetch_map(&P.bank[b].ak2);
         tma_prefetch_map(&P.bank[b].bk);
-        tma_prefetch_map(&P.bank[b].bk2);
       }
+      const uint32_t full_even = map_to_rank(&full[0], 0);
       int st = 0;
       uint32_t ph = 0;
       uint32_t it = 0;
       for (uint32_t k = 0;; ++k) {
-        const int s = k % TASK_SLOTS;
-        if (!mbar_wait_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
-          fail();
-          break;
-        }
-        const Task tk = rec[s];
-        mbar_arrive(&prod_took[s]);
-        mbar_arrive(&slot_empty[s]);
+        Task tk;
+        if (!read_slot(k, tk)) break;
+        if (even) mbar_arrive(&prod_took[k % TASK_SLOTS]);
+        release_slot(k % TASK_SLOTS);
         if (tk.t < 0 || *abort_flag) break;
         // the scheduler acquired the inputs of this task; order them before this thread's TMA reads
         fence_proxy_async_global();
         const Operands op = task_operands(P.bank[tk.bi], tk);
         const int KB = (op.K + BK - 1) / BK;
-        const uint32_t bytes = A_TILE_BYTES + tk.nt * BK * 2;
-        const int ma = tk.m0 >> 6, nb = tk.n0 >> 6;
+        const int m0 = tk.m0 + static_cast<int>(rank) * BM;         // this CTA's A rows
+        const int nb0 = tk.n0 + static_cast<int>(rank) * (tk.nt >> 1);   // this CTA's B rows
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          if (it >= STAGES && !mbar_wait_or_abort(&empty[st], ph ^ 1u, abort_flag)) {
+          if (it >= STAGES && !mbar_wait_cluster_or_abort(&empty[st], ph ^ 1u, abort_flag)) {
             fail();
             ok = false;
             break;
           }
-          mbar_expect_tx(&full[st], bytes);
+          if (even) mbar_expect_tx(&full[st], 2u * STAGE_BYTES);   // both CTAs' boxes
+          const uint32_t fb = full_even + 8u * static_cast<uint32_t>(st);
           uint8_t* a = sA + st * A_TILE_BYTES;
-          uint8_t* b = sB + st * B_TILE_BYTES;
+          uint8_t* b = sB + st * BH_TILE_BYTES;
           const int k0 = kb * BK;
-          if (!op.a_mn) tma_load_3d(a, op.a, &full[st], k0, tk.m0, tk.mat);
-          else tma_load_4d(a, op.a, &full[st], 0, k0, ma, tk.mat);
-          if (!op.b_mn) tma_load_3d(b, op.b, &full[st], k0, tk.n0, tk.mat);
-          else tma_load_4d(b, op.b, &full[st], 0, k0, nb, tk.mat);
+          if (!op.a_mn) tma_load_3d_pair(a, op.a, fb, k0, m0, tk.mat);
+          else tma_load_4d_pair(a, op.a, fb, 0, k0, m0 >> 6, tk.mat);
+          if (!op.b_mn) tma_load_3d_pair(b, op.b, fb, k0, nb0, tk.mat);
+          else tma_load_4d_pair(b, op.b, fb, 0, k0, nb0 >> 6, tk.mat);
           if (++st == STAGES) {
             st = 0;
             ph ^= 1u;
@@ -540,30 +604,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         }
         if (!ok) break;
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      uint32_t it = 0;
-      for (uint32_t k = 0;; ++k) {
-        const int s = k % TASK_SLOTS;
-        if (!mbar_wait_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
+      // this CTA stays until the multicast releases of every stage it filled have arrived
+      for (uint32_t i = it > STAGES ? it - STAGES : 0u; i < it; ++i) {
+        if (!mbar_wait_cluster_or_abort(&empty[i % STAGES], (i / STAGES) & 1, abort_flag)) {
           fail();
           break;
         }
-        const Task tk = rec[s];
-        mbar_arrive(&slot_empty[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (even && lane == 0) {
+      // ---------------- MMA issuer of the pair
+      uint32_t it = 0;
+      for (uint32_t k = 0;; ++k) {
+        Task tk;
+        if (!read_slot(k, tk)) break;
+        release_slot(k % TASK_SLOTS);
         if (tk.t < 0 || *abort_flag) break;
         const Operands op = task_operands(P.bank[tk.bi], tk);
         const int KB = (op.K + BK - 1) / BK;
         const uint32_t buf = k & 1;
-        if (k >= 2 && !mbar_wait_or_abort(&tempty[buf], ((k >> 1) - 1) & 1, abort_flag)) {
+        if (k >= 2 && !mbar_wait_cluster_or_abort(&tempty[buf], ((k >> 1) - 1) & 1, abort_flag)) {
           fail();
           break;
         }
         tc_fence_after();
         const uint32_t dacc = tmem + buf * ACC_COLS;
-        const uint32_t idesc = idesc_bf16_m128(tk.nt, op.a_mn, op.b_mn);
+        const uint32_t idesc = idesc_bf16_m256(tk.nt, op.a_mn, op.b_mn);
         const uint32_t a_step = op.a_mn ? 2048u : 32u, b_step = op.b_mn ? 2048u : 32u;
         const uint32_t a_lbo = op.a_mn ? 8192u : 16u, b_lbo = op.b_mn ? 8192u : 16u;
         bool ok = true;
@@ -575,15 +642,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + st * A_TILE_BYTES), b0 = smem_u32(sB + st * B_TILE_BYTES);
+          const uint32_t a0 = smem_u32(sA + st * A_TILE_BYTES), b0 = smem_u32(sB + st * BH_TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            umma_bf16(dacc, smem_desc_sw128(a0 + kk * a_step, a_lbo, 1024),
-                      smem_desc_sw128(b0 + kk * b_step, b_lbo, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(dacc, smem_desc_sw128(a0 + kk * a_step, a_lbo, 1024),
+                           smem_desc_sw128(b0 + kk * b_step, b_lbo, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[st]);
+          umma_commit_pair_both(&empty[st]);   // the stage may be refilled in both CTAs
         }
-        umma_commit(&tfull[buf]);
+        umma_commit_pair_both(&tfull[buf]);
         if (!ok) break;
       }
     }
@@ -593,15 +660,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     uint8_t* ebuf = sEpi + (warp - 2) * EPI_BUF_BYTES;
+    const uint32_t tempty_even = map_to_rank(&tempty[0], 0);
     for (uint32_t k = 0;; ++k) {
-      const int s = k % TASK_SLOTS;
-      if (!mbar_wait_or_abort(&slot_full[s], (k / TASK_SLOTS) & 1, abort_flag)) {
-        fail();
-        break;
-      }
-      const Task tk = rec[s];
+      Task tk;
+      if (!read_slot(k, tk)) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&slot_empty[s]);
+      if (lane == 0) release_slot(k % TASK_SLOTS);
       if (tk.t < 0) break;
       const NsBank& B = P.bank[tk.bi];
       const uint32_t buf = k & 1;
@@ -619,7 +683,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       EpiJob J;
       J.mat = tk.mat;
       J.it = tk.it;
-      J.m0 = tk.m0;
+      J.m0 = tk.m0 + static_cast<int>(rank) * BM;   // this CTA's rows of the pair tile
       J.n0 = tk.n0;
       J.nt = tk.nt;
       J.alpha = 1.f;
@@ -666,7 +730,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&tempty[buf]);
+        mbar_arrive_remote(tempty_even + 8u * buf);    // the even CTA's MMA issuer may reuse the accumulator
         bulk_wait_all();                         // this warp's part of the tile is in global memory
         mbar_arrive(tile_done);
       }
@@ -687,16 +751,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();      // no multicast or remote arrival targets a CTA that has left
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
 // per-device launch set-up, done by the first call on each device (concurrent first calls
 // from several host threads do the same idempotent work)
 std::atomic<bool> g_attr_done[64];
-std::atomic<int> g_num_sms[64];
+std::atomic<int> g_max_clusters[64];
 
 }  // namespace
 
@@ -712,14 +777,30 @@ cudaError_t launch_ns_fused(const NsParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     g_attr_done[dev].store(true, std::memory_order_release);
   }
-  int nsm = g_num_sms[dev].load(std::memory_order_relaxed);
-  if (nsm == 0) {
-    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = GEMM_SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int npairs = g_max_clusters[dev].load(std::memory_order_relaxed);
+  if (npairs == 0) {
+    // one pair per two SMs, as many as can be resident at once (every pair must be)
+    cfg.gridDim = dim3(2, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&npairs, reinterpret_cast<const void*>(ns_fused_kernel), &cfg);
     if (e != cudaSuccess) return e;
-    g_num_sms[dev].store(nsm, std::memory_order_relaxed);
+    if (npairs <= 0) return cudaErrorInvalidConfiguration;
+    g_max_clusters[dev].store(npairs, std::memory_order_relaxed);
   }
-  const int grid = p.total_tasks < nsm ? p.total_tasks : nsm;
-  ns_fused_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(p);
+  const int pairs = p.total_tasks < npairs ? p.total_tasks : npairs;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, ns_fused_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -39,7 +39,8 @@ def test_version_and_status_strings(lib):
     assert lib.mb_version() >> 16 == 1
     from newton_schulz_stacked_gb300 import _binding as b
     for code in (b.MB_OK, b.MB_ERR_NULL, b.MB_ERR_SHAPE, b.MB_ERR_ALIGN, b.MB_ERR_NS_STEPS, b.MB_ERR_WORKSPACE,
-                 b.MB_ERR_CUDA, b.MB_ERR_TIMEOUT, b.MB_ERR_ARG, b.MB_ERR_UNSUPPORTED, b.MB_ERR_TOO_MANY):
+                 b.MB_ERR_CUDA, b.MB_ERR_TIMEOUT, b.MB_ERR_ARG, b.MB_ERR_UNSUPPORTED, b.MB_ERR_TOO_MANY,
+                 b.MB_ERR_SCRATCH_LIMIT, b.MB_ERR_DEVICE):
         assert lib.mb_status_string(code)
     assert lib.mb_status_string(12345) == b"unknown status"
 
