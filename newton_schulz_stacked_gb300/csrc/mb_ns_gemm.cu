@@ -16,7 +16,8 @@
 // half of the B operand's nt rows, and its TMEM receives its 128 rows x all nt
 // columns.  Each SM therefore stages 32 KB of operands per 64-deep k-block
 // instead of 48 KB for a 128 x 256 tile alone: a third less L2-to-SM traffic,
-// and six stages in flight where four fitted before.
+// and five stages in flight where four fitted before, with room left for the
+// epilogue's input ring.
 //
 // A and B are symmetric: GRAM and POLY compute only the 256 x 256 tiles (2 x 2
 // aligned 128-blocks) that touch the upper triangle.  Each block above the
@@ -54,8 +55,9 @@
 //                   releases each stage in both CTAs with a multicast commit
 //   warps 2..9    : epilogue of the CTA's own 128 rows, two warps per 32-lane
 //                   TMEM quadrant (each takes half the columns); task k's
-//                   epilogue runs under task k+1's MMAs; results leave through
-//                   shared memory by TMA bulk stores
+//                   epilogue runs under task k+1's MMAs; its input (A for POLY,
+//                   X for APPLY) arrives by TMA in 32x32 chunks a chunk ahead,
+//                   and its results leave through shared memory by TMA bulk stores
 #include <atomic>
 
 #include "mb_device.cuh"
@@ -67,7 +69,7 @@ namespace {
 
 constexpr int BM = 128;                      // rows of a tile per CTA
 constexpr int BK = 64;
-constexpr int STAGES = 6;
+constexpr int STAGES = 5;
 constexpr int A_TILE_BYTES = BM * BK * 2;    // 16 KB
 constexpr int BH_TILE_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of a 256-row B operand
 constexpr int STAGE_BYTES = A_TILE_BYTES + BH_TILE_BYTES;
@@ -75,13 +77,17 @@ constexpr int TILE_SMEM = STAGES * STAGE_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_BUF_BYTES = 4096;          // per epilogue warp: 32x32 bf16 chunk + its transpose
 constexpr int EPI_SMEM = EPI_WARPS * EPI_BUF_BYTES;
+constexpr int IN_SLOTS = 2;                  // per epilogue warp: input chunks in flight
+constexpr int IN_BOX_BYTES = 32 * 32 * 2;    // one 32x32 bf16 input chunk
+constexpr int IN_SMEM = EPI_WARPS * IN_SLOTS * IN_BOX_BYTES;
 constexpr int TASK_SLOTS = 4;                // claimed tasks in flight inside a pair
 // threads that read a task record and arrive on their own CTA's slot_empty barrier: in the
 // even CTA its producer, the MMA issuer, its epilogue warps and the odd CTA's relay; in the
 // odd CTA its producer and epilogue warps
 constexpr int SLOT_READERS_EVEN = 1 + 1 + EPI_WARPS + 1;
 constexpr int SLOT_READERS_ODD = 1 + EPI_WARPS;
-constexpr int GEMM_SMEM = TILE_SMEM + EPI_SMEM + 1024 /* alignment slack */ + 512 /* barriers, slots */;
+constexpr int GEMM_SMEM = TILE_SMEM + EPI_SMEM + IN_SMEM + 1024 /* alignment slack */ + 768 /* barriers, slots */;
+static_assert(GEMM_SMEM <= 232448, "shared memory per CTA");
 constexpr int SCHED_WARP = 2 + EPI_WARPS;
 constexpr int GEMM_THREADS = 32 * (3 + EPI_WARPS);
 constexpr uint32_t ACC_COLS = 256;           // one accumulator
@@ -258,8 +264,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float
 
 struct EpiJob {
   const CUtensorMap* st;   // store map of the output
-  const uint16_t* ein;     // epilogue input of this matrix (A for POLY, X for APPLY)
-  long long ein_ld;
+  long long ein_ld;        // row pitch of the matrix the epilogue input comes from
   // APPLY only: the first step also stores the bf16 residual of X_1 (st_lo), and the
   // second step adds it back (ein_lo) so that its a*X_1 term uses X_1 to ~16 bits
   const CUtensorMap* st_lo;
@@ -273,18 +278,107 @@ struct EpiJob {
 // step); LO_READ adds the residual stored by the first step to its a*X term (second step).
 constexpr int LO_WRITE = 1, LO_READ = 2;
 
+// Non-blocking: whether the phase with the given parity has completed (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Where one epilogue warp's input of a task comes from: chunk c is the 32x32 box at
+// (col0 + 32 c, row0) of matrix `mat` of A (POLY) or X (APPLY), read through the map that
+// the phase which wrote it stored with (64-byte swizzle, so a lane reading its own row of
+// the box hits distinct banks).  Boxes reaching past the matrix read zeros.
+struct InSrc {
+  const CUtensorMap* map;
+  int row0, col0, mat, nch;
+};
+
+__device__ __forceinline__ InSrc input_of(const NsParams& P, const Task& tk, int row_base, int half) {
+  InSrc s{nullptr, 0, 0, 0, 0};
+  if (tk.t < 0 || tk.ph == EPI_GRAM) return s;
+  const NsBank& B = P.bank[tk.bi];
+  s.map = tk.ph == EPI_POLY ? &B.st_a : &B.st_x[iterate_buffer(tk.it)];
+  s.row0 = tk.m0 + row_base;
+  s.col0 = tk.n0 + half * (tk.nt >> 1);
+  s.mat = tk.mat;
+  s.nch = tk.nt >> 6;   // (nt / 2) columns in 32-column chunks
+  return s;
+}
+
+// One epilogue warp's input ring: IN_SLOTS shared buffers that TMA fills up to
+// IN_SLOTS - 1 chunks ahead of their use.  Once a task's chunks are all issued, the ring
+// runs on into the next task's as soon as that task's record is published (a
+// non-blocking test: the next task may depend on this one).  The counters are
+// warp-uniform; lane 0 issues.
+struct InFeed {
+  uint8_t* buf;            // IN_SLOTS x IN_BOX_BYTES
+  uint64_t* full;          // IN_SLOTS barriers: lane 0's expect_tx arrival, then the bytes
+  const Task* rec;         // the task records ...
+  uint64_t* slot_full;     // ... and their barriers
+  uint32_t k;              // the task this warp is working on
+  uint32_t issued, used;   // chunks issued and consumed so far
+  InSrc cur, nxt;          // the inputs of task k and task k + 1
+  int cur_iss, nxt_iss;    // how many of their chunks are issued
+  bool nxt_known;
+  int row_base, half;      // this warp's rows (CTA rank and quadrant) and column half
+};
+
+__device__ __forceinline__ void in_issue(InFeed& F, const InSrc& s, int c, int lane) {
+  if (lane == 0) {
+    const uint32_t slot = F.issued % IN_SLOTS;
+    mbar_expect_tx(&F.full[slot], IN_BOX_BYTES);
+    tma_load_3d(F.buf + slot * IN_BOX_BYTES, s.map, &F.full[slot], s.col0 + 32 * c, s.row0, s.mat);
+  }
+  ++F.issued;
+}
+
+// Issues input chunks while the ring has room: the rest of task k's, then task k + 1's.
+// A slot is refilled only after the chunk it held was consumed (every lane used the
+// values before the warp got here).
+__device__ __forceinline__ void in_top_up(InFeed& F, const NsParams& P, int lane) {
+  while (F.issued - F.used < static_cast<uint32_t>(IN_SLOTS)) {
+    if (F.cur_iss < F.cur.nch) {
+      in_issue(F, F.cur, F.cur_iss++, lane);
+      continue;
+    }
+    if (!F.nxt_known) {
+      const uint32_t k1 = F.k + 1;
+      // every lane acquires the record's publication itself before reading it
+      const bool ready =
+          __all_sync(0xffffffffu, mbar_test_cluster(&F.slot_full[k1 % TASK_SLOTS], (k1 / TASK_SLOTS) & 1));
+      if (!ready) return;
+      F.nxt = input_of(P, F.rec[k1 % TASK_SLOTS], F.row_base, F.half);
+      F.nxt_iss = 0;
+      F.nxt_known = true;
+      // the scheduler acquired the task's inputs; order them before this thread's TMA reads
+      if (lane == 0) fence_proxy_async_global();
+    }
+    if (F.nxt_iss >= F.nxt.nch) return;
+    in_issue(F, F.nxt, F.nxt_iss++, lane);
+  }
+}
+
 // Epilogue of one warp: TMEM lanes of quadrant `quad` (tile rows quad*32 + lane),
 // columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`, taken
-// 16 columns at a time with the next 16 columns' input prefetched.
+// 16 columns at a time.
 // Each 32x32 chunk is staged in the warp's shared buffer and written with a
 // TMA bulk store; a symmetric phase also stores the transposed chunk at the
 // mirrored position.  A 128-block below the diagonal is not stored at all; in
 // a diagonal 128-block the chunks below the diagonal are not stored (their
 // mirror covers them) and the chunk on the diagonal is made symmetric before
 // its store, so every element is written exactly once.
+// The input (A for POLY, X for APPLY) comes through the warp's input ring; false if a wait
+// for it ran out.
 template <int EPI, int LO>
-__device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uint32_t tacc, int quad, int half,
-                                         int lane, uint8_t* ebuf) {
+__device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uint32_t tacc, int quad, int half,
+                                         int lane, uint8_t* ebuf, InFeed& F, const volatile int* abort_flag) {
   constexpr bool has_ein = EPI != EPI_GRAM;
   constexpr bool with_lo = EPI == EPI_APPLY && LO == LO_READ;
   uint8_t* bufD = ebuf;          // [32 rows][32 cols] bf16, 64-byte swizzle
@@ -300,8 +394,7 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
   const uint32_t word_off = 4u * ((lane >> 1) & 3);
   const float ca = P.ca[J.it], cb = P.cb[J.it], cc = P.cc[J.it];
 
-  uint32_t e_cur[8], e_nxt[8], l_cur[8], l_nxt[8];
-  if (has_ein) load_row16_raw(J.ein, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, e_cur);
+  uint32_t l_cur[8], l_nxt[8];
   if (with_lo) load_row16_raw(J.ein_lo, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, l_cur);
 
   for (int c = 0; c < ncols; c += 32) {
@@ -323,13 +416,26 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
     }
     const bool lo_out = EPI == EPI_APPLY && LO == LO_WRITE && direct;
 
+    const uint8_t* in = nullptr;
+    if (has_ein) {
+      in_top_up(F, P, lane);
+      const uint32_t slot = F.used % IN_SLOTS;
+      if (!mbar_wait_or_abort(&F.full[slot], (F.used / IN_SLOTS) & 1, abort_flag)) return false;
+      in = F.buf + slot * IN_BOX_BYTES;
+    }
     if (lane == 0) bulk_wait_read_all();        // the previous chunk's stores have read the buffers
     __syncwarp();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int hc = col0 + 16 * h;
       const bool more = c + 16 * h + 16 < ncols;
-      if (has_ein && more) load_row16_raw(J.ein, J.ein_ld, row, hc + 16, J.N, row_ok, e_nxt);
+      uint32_t e_cur[8];
+      if (has_ein) {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(in + sw64(lane, 2 * h));
+        const uint4 v1 = *reinterpret_cast<const uint4*>(in + sw64(lane, 2 * h + 1));
+        e_cur[0] = v0.x; e_cur[1] = v0.y; e_cur[2] = v0.z; e_cur[3] = v0.w;
+        e_cur[4] = v1.x; e_cur[5] = v1.y; e_cur[6] = v1.z; e_cur[7] = v1.w;
+      }
       if (with_lo && more) load_row16_raw(J.ein_lo, J.ein_ld, row, hc + 16, J.N, row_ok, l_nxt);
       uint32_t acc[16];
       tmem_ld_32x16(tacc + lane_base + static_cast<uint32_t>(cbeg + c + 16 * h), acc);
@@ -382,10 +488,6 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
         *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
         *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
       }
-      if (has_ein && more) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) e_cur[i] = e_nxt[i];
-      }
       if (with_lo && more) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) l_cur[i] = l_nxt[i];
@@ -411,6 +513,7 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
         *reinterpret_cast<uint4*>(bufD + sw64(lane, j)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
       }
     }
+    if (has_ein) ++F.used;                      // its slot is refilled no earlier than the next top-up
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && (direct || mirror)) {
@@ -420,6 +523,7 @@ __device__ __forceinline__ void epilogue(const NsParams& P, const EpiJob& J, uin
       bulk_commit();
     }
   }
+  return true;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -430,7 +534,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_TILE_BYTES;
   uint8_t* sEpi = smem + TILE_SMEM;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TILE_SMEM + EPI_SMEM);  // [STAGES] (even) both halves landed
+  uint8_t* sIn = sEpi + EPI_SMEM;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sIn + IN_SMEM);  // [STAGES] (even) both halves landed
   uint64_t* empty = full + STAGES;                // [STAGES] the pair's MMAs are done with the stage
   uint64_t* tfull = empty + STAGES;               // [2] accumulator ready for the epilogue
   uint64_t* tempty = tfull + 2;                   // [2] (even) both CTAs' epilogues drained the accumulator
@@ -438,7 +543,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
   uint64_t* slot_empty = slot_full + TASK_SLOTS;  // [TASK_SLOTS] (even) every reader of both CTAs has it
   uint64_t* prod_took = slot_empty + TASK_SLOTS;  // [TASK_SLOTS] (even) the even producer has started the task
   uint64_t* tile_done = prod_took + TASK_SLOTS;   // every epilogue warp's stores of a task are complete
-  Task* rec = reinterpret_cast<Task*>(tile_done + 2);   // [TASK_SLOTS] (16-byte aligned)
+  uint64_t* in_full = tile_done + 2;              // [EPI_WARPS][IN_SLOTS] epilogue input chunk landed
+  Task* rec = reinterpret_cast<Task*>(in_full + EPI_WARPS * IN_SLOTS);   // [TASK_SLOTS] (16-byte aligned)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rec + TASK_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -461,6 +567,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       mbar_init(&prod_took[s], 1);
     }
     mbar_init(tile_done, EPI_WARPS);
+    for (int i = 0; i < EPI_WARPS * IN_SLOTS; ++i) mbar_init(&in_full[i], 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -661,12 +768,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
     const int half = (warp - 2) >> 2;
     uint8_t* ebuf = sEpi + (warp - 2) * EPI_BUF_BYTES;
     const uint32_t tempty_even = map_to_rank(&tempty[0], 0);
+    InFeed F;
+    F.buf = sIn + (warp - 2) * IN_SLOTS * IN_BOX_BYTES;
+    F.full = in_full + (warp - 2) * IN_SLOTS;
+    F.rec = rec;
+    F.slot_full = slot_full;
+    F.issued = F.used = 0;
+    F.cur_iss = F.nxt_iss = 0;
+    F.cur.nch = F.nxt.nch = 0;
+    F.nxt_known = false;
+    F.row_base = static_cast<int>(rank) * BM + quad * 32;
+    F.half = half;
     for (uint32_t k = 0;; ++k) {
       Task tk;
       if (!read_slot(k, tk)) break;
+      // the input of task k: already known (and partly issued) if the ring ran ahead into it
+      F.k = k;
+      if (F.nxt_known) {
+        F.cur = F.nxt;
+        F.cur_iss = F.nxt_iss;
+        F.nxt_known = false;
+      } else {
+        F.cur = input_of(P, tk, F.row_base, half);
+        F.cur_iss = 0;
+        if (lane == 0) fence_proxy_async_global();
+      }
       __syncwarp();
       if (lane == 0) release_slot(k % TASK_SLOTS);
       if (tk.t < 0) break;
+      in_top_up(F, P, lane);                     // this task's first input chunks, under its MMAs
       const NsBank& B = P.bank[tk.bi];
       const uint32_t buf = k & 1;
       if (!mbar_wait_or_abort(&tfull[buf], (k >> 1) & 1, abort_flag)) {
@@ -675,11 +805,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       }
       if (*abort_flag) break;
       tc_fence_after();
-      // make the epilogue inputs visible to this warp: A (POLY reads what GRAM wrote) and
-      // X (APPLY reads the previous step's APPLY output)
-      int dit, dph;
-      if (dependency(tk, dit, dph)) ld_acquire(done_counter(B, tk.mat, dit, dph));
-      if (tk.ph == EPI_APPLY && tk.it > 0) ld_acquire(done_counter(B, tk.mat, tk.it - 1, EPI_APPLY));
       EpiJob J;
       J.mat = tk.mat;
       J.it = tk.it;
@@ -690,28 +815,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       J.st_lo = nullptr;
       J.ein_lo = nullptr;
       const uint32_t tacc = tmem + buf * ACC_COLS;
+      bool ok;
       if (tk.ph == EPI_GRAM) {
         if (tk.it == 0) {
           const float sc = B.scale[tk.mat];
           J.alpha = sc * sc;
         }
         J.st = &B.st_a;
-        J.ein = nullptr;
         J.ein_ld = 0;
         J.M = J.N = B.m;
         J.sym = 1;
-        epilogue<EPI_GRAM, 0>(P, J, tacc, quad, half, lane, ebuf);
+        ok = epilogue<EPI_GRAM, 0>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
       } else if (tk.ph == EPI_POLY) {
         J.st = &B.st_b;
-        J.ein = B.a + tk.mat * B.m_ms;
         J.ein_ld = B.m_ld;
         J.M = J.N = B.m;
         J.sym = 1;
-        epilogue<EPI_POLY, 0>(P, J, tacc, quad, half, lane, ebuf);
+        ok = epilogue<EPI_POLY, 0>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
       } else {
         if (tk.it == 0) J.alpha = B.scale[tk.mat];
         J.st = &B.st_x[iterate_buffer(tk.it + 1)];
-        J.ein = B.x[iterate_buffer(tk.it)] + tk.mat * B.x_ms;
         J.ein_ld = B.x_ld;
         // X_1's residual waits in x[2], which the second APPLY overwrites tile by tile only
         // after each tile has read its own part
@@ -721,12 +844,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         J.N = B.tall ? B.m : B.n;
         J.sym = 0;
         if (J.st_lo)
-          epilogue<EPI_APPLY, LO_WRITE>(P, J, tacc, quad, half, lane, ebuf);
+          ok = epilogue<EPI_APPLY, LO_WRITE>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
         else if (J.ein_lo)
-          epilogue<EPI_APPLY, LO_READ>(P, J, tacc, quad, half, lane, ebuf);
+          ok = epilogue<EPI_APPLY, LO_READ>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
         else
-          epilogue<EPI_APPLY, 0>(P, J, tacc, quad, half, lane, ebuf);
+          ok = epilogue<EPI_APPLY, 0>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
       }
+      if (!ok) {
+        fail();
+        break;
+      }
+      in_top_up(F, P, lane);                     // the next task's first chunks, under this one's store waits
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -746,6 +874,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       }
       __syncwarp();
     }
+    // input chunks still in flight (only after an abort) land before the CTA exits
+    for (; F.used != F.issued; ++F.used)
+      if (!mbar_wait(&F.full[F.used % IN_SLOTS], (F.used / IN_SLOTS) & 1)) break;
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
