@@ -84,6 +84,9 @@ def test_update_bit_exact_cases(nss):
 NS_SHAPES = [
     ((4, 128, 128), "gauss"), ((2, 256, 384), "gauss"), ((2, 384, 256), "gauss"),
     ((2, 200, 328), "gauss"), ((2, 328, 200), "gauss"), ((2, 65, 130), "gauss"), ((2, 130, 65), "gauss"),
+    # three 128-blocks per side of A: the second 256-row pair tile has a partial even CTA and an
+    # odd CTA wholly past the matrix; 520 columns end in an 8-column tile
+    ((2, 300, 520), "gauss"), ((2, 520, 300), "lowrank"),
     ((2, 768, 768), "lowrank"), ((1, 768, 3072), "gauss"), ((2, 3072, 768), "lowrank"),
     ((3, 12, 768), "lowrank"), ((3, 6, 12), "lowrank"), ((2, 64, 64), "gauss"), ((2, 1, 40), "gauss"),
     # small min(rows, cols) whose fp32 iteration does not fit in shared memory: workspace path
