@@ -59,7 +59,14 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
 
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         results = list(ex.map(compile_one, zip(srcs, objs)))
-    for cmd, r in results:
+    for i, (cmd, r) in enumerate(results):
+        # a compiler process that crashed (seen as a segmentation fault of nvcc on a loaded
+        # build host) is retried on its own before the build gives up
+        for _ in range(2):
+            if r.returncode == 0:
+                break
+            sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr + "retrying this file alone\n")
+            cmd, r = compile_one((srcs[i], objs[i]))
         if verbose or r.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         if r.returncode != 0:
