@@ -60,9 +60,10 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         results = list(ex.map(compile_one, zip(srcs, objs)))
     for i, (cmd, r) in enumerate(results):
-        # a compiler process that crashed (seen as a segmentation fault of nvcc on a loaded
-        # build host) is retried on its own before the build gives up
-        for _ in range(2):
+        # the compiler's NVVM stage (cicc) on the aarch64 hosts sometimes dies with a
+        # segmentation fault on this source (about one compile in six to one in three, on the
+        # same inputs); a crashed file is retried on its own before the build gives up
+        for _ in range(4):
             if r.returncode == 0:
                 break
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr + "retrying this file alone\n")
