@@ -32,7 +32,8 @@ sys.path.insert(0, ROOT)
 METRIC = "Muon bank-steps/sec & NS TFLOP/s vs bf16 peak; update GB/s vs HBM peak"
 UNIT = "bank-steps/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-NS_GEMM_SOURCES = ["newton_schulz_stacked_gb300/csrc/mb_ns_gemm.cu", "newton_schulz_stacked_gb300/csrc/mb_device.cuh"]
+NS_GEMM_SOURCES = ["newton_schulz_stacked_gb300/csrc/mb_ns_gemm.cu", "newton_schulz_stacked_gb300/csrc/mb_device.cuh",
+                   "newton_schulz_stacked_gb300/csrc/mb_internal.h"]
 
 
 def parse():
