@@ -9,6 +9,7 @@ torch only when the caller does not pass one.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 from typing import Optional, Sequence
 
@@ -19,8 +20,9 @@ from ._binding import MuonBankError, MB_MAX_BANKS  # noqa: F401
 
 __all__ = [
     "muon_bank_step", "normuon_bank_step", "muon_multi_step", "mb_workspace_bytes",
-    "mb_multi_workspace_bytes", "mb_momentum", "mb_newton_schulz", "mb_update", "mb_normuon_update",
-    "mb_newton_schulz_noalloc", "mb_workspace_views", "mb_sync_status", "mb_selftest_timeout", "mb_status_string", "MuonBankError",
+    "mb_multi_workspace_bytes", "muon_multi_step_dev", "mb_momentum", "mb_newton_schulz",
+    "mb_newton_schulz_coeffs", "mb_update", "mb_normuon_update", "mb_newton_schulz_noalloc", "mb_workspace_views",
+    "mb_sync_status", "mb_selftest_timeout", "mb_status_string", "MuonBankError",
     "BankState", "load_library", "mb_launch_count", "StageTimer",
 ]
 
@@ -43,6 +45,23 @@ def _ptr(t: Optional[torch.Tensor], dtypes, what: str) -> Optional[int]:
     return t.data_ptr()
 
 
+def _same(what: str, ref: torch.Tensor, t: Optional[torch.Tensor], numel: Optional[int] = None):
+    """The kernels index every tensor of a call with one shape: a tensor of another size or
+    on another device would be read or written out of bounds, so it is refused here."""
+    if t is None:
+        return
+    want = ref.numel() if numel is None else numel
+    if t.numel() != want:
+        raise ValueError(f"{what} has {t.numel()} elements, expected {want}")
+    if t.device != ref.device:
+        raise ValueError(f"{what} is on {t.device}, the call's tensors are on {ref.device}")
+
+
+def _on(t: torch.Tensor):
+    """Runs the call with the tensors' device current (the library launches on the current device)."""
+    return torch.cuda.device(t.device) if t.is_cuda else contextlib.nullcontext()
+
+
 def _shape(t: torch.Tensor) -> _b.MbShape:
     if t.dim() == 2:
         return _b.shape_of(1, t.shape[0], t.shape[1])
@@ -60,6 +79,10 @@ def _stream(stream) -> int:
 def _workspace(nbytes: int, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
     if workspace is None:
         return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    if not workspace.is_cuda or workspace.device != torch.device(device):
+        raise ValueError(f"workspace must be a CUDA tensor on {device}")
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
     if workspace.numel() * workspace.element_size() < nbytes:
         raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, needs {nbytes}")
     return workspace
@@ -79,11 +102,14 @@ def muon_bank_step(bank, grad, momentum, mantissa, lr: float, wd: float, mu: flo
                    workspace=None, stream=None):
     """One Muon step over the bank, in place (bank, momentum, mantissa)."""
     sh = _shape(bank)
+    for name, t in (("grad", grad), ("momentum", momentum), ("mantissa", mantissa)):
+        _same(name, bank, t)
     ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols)), workspace, bank.device)
-    st = _b.load().muon_bank_step(
-        _ptr(bank, _TWO_BYTE, "bank"), _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"),
-        _ptr(mantissa, _TWO_BYTE, "mantissa"), sh, lr, wd, mu, ns_steps, ws.data_ptr(),
-        ws.numel() * ws.element_size(), _stream(stream))
+    with _on(bank):
+        st = _b.load().muon_bank_step(
+            _ptr(bank, _TWO_BYTE, "bank"), _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"),
+            _ptr(mantissa, _TWO_BYTE, "mantissa"), sh, lr, wd, mu, ns_steps, ws.data_ptr(),
+            ws.numel() * ws.element_size(), _stream(stream))
     _b.check("muon_bank_step", st)
     return ws
 
@@ -92,11 +118,15 @@ def normuon_bank_step(bank, grad, momentum, mantissa, row_state, lr: float, wd: 
                       beta2: float = 0.95, ns_steps: int = 5, workspace=None, stream=None):
     """One Muon step with NorMuon per-row normalisation, in place (row_state too)."""
     sh = _shape(bank)
+    for name, t in (("grad", grad), ("momentum", momentum), ("mantissa", mantissa)):
+        _same(name, bank, t)
+    _same("row_state", bank, row_state, sh.batch * sh.rows)
     ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols), True), workspace, bank.device)
-    st = _b.load().normuon_bank_step(
-        _ptr(bank, _TWO_BYTE, "bank"), _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"),
-        _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(row_state, (torch.float32,), "row_state"), sh, lr, wd, mu,
-        beta2, ns_steps, ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+    with _on(bank):
+        st = _b.load().normuon_bank_step(
+            _ptr(bank, _TWO_BYTE, "bank"), _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"),
+            _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(row_state, (torch.float32,), "row_state"), sh, lr, wd, mu,
+            beta2, ns_steps, ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
     _b.check("normuon_bank_step", st)
     return ws
 
@@ -108,6 +138,11 @@ class BankState:
         self.bank, self.grad, self.momentum, self.mantissa, self.row_state = bank, grad, momentum, mantissa, row_state
 
     def desc(self) -> _b.MbBankDesc:
+        for name, t in (("grad", self.grad), ("momentum", self.momentum), ("mantissa", self.mantissa)):
+            _same(name, self.bank, t)
+        if self.row_state is not None:
+            sh = _shape(self.bank)
+            _same("row_state", self.bank, self.row_state, sh.batch * sh.rows)
         return _b.MbBankDesc(_ptr(self.bank, _TWO_BYTE, "bank"), _ptr(self.grad, _TWO_BYTE, "grad"),
                              _ptr(self.momentum, (torch.float32,), "momentum"),
                              _ptr(self.mantissa, _TWO_BYTE, "mantissa"),
@@ -115,6 +150,11 @@ class BankState:
 
 
 def _descs(banks: Sequence[BankState]):
+    if len(banks) == 0:
+        raise ValueError("no banks")
+    for b in banks[1:]:
+        if b.bank.device != banks[0].bank.device:
+            raise ValueError("all banks of one call must be on one device")
     arr = (_b.MbBankDesc * len(banks))()
     for i, b in enumerate(banks):
         arr[i] = b.desc()
@@ -133,8 +173,9 @@ def muon_multi_step(banks: Sequence[BankState], lr: float, wd: float, mu: float,
     """One step over several banks as one launch sequence."""
     arr = _descs(banks)
     ws = _workspace(mb_multi_workspace_bytes(banks, normuon), workspace, banks[0].bank.device)
-    st = _b.load().muon_multi_step(arr, len(banks), lr, wd, mu, int(normuon), beta2, ns_steps, ws.data_ptr(),
-                                   ws.numel() * ws.element_size(), _stream(stream))
+    with _on(banks[0].bank):
+        st = _b.load().muon_multi_step(arr, len(banks), lr, wd, mu, int(normuon), beta2, ns_steps, ws.data_ptr(),
+                                       ws.numel() * ws.element_size(), _stream(stream))
     _b.check("muon_multi_step", st)
     return ws
 
@@ -151,42 +192,51 @@ def muon_multi_step_dev(banks: Sequence[BankState], scalars, normuon: bool = Fal
             and scalars.is_contiguous() and scalars.numel() == 4 * len(banks)):
         raise ValueError("scalars must be a contiguous CUDA float32 tensor of 4 values per bank")
     arr = _descs(banks)
+    if scalars.device != banks[0].bank.device:
+        raise ValueError("scalars must be on the banks' device")
     ws = _workspace(mb_multi_workspace_bytes(banks, normuon), workspace, banks[0].bank.device)
-    st = _b.load().muon_multi_step_dev(arr, len(banks), scalars.data_ptr(), int(normuon), ns_steps, ws.data_ptr(),
-                                       ws.numel() * ws.element_size(), _stream(stream))
+    with _on(banks[0].bank):
+        st = _b.load().muon_multi_step_dev(arr, len(banks), scalars.data_ptr(), int(normuon), ns_steps,
+                                           ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
     _b.check("muon_multi_step_dev", st)
     return ws
 
 
 def mb_momentum(grad, momentum, u, mu: float, stream=None):
     sh = _shape(grad)
-    _b.check("mb_momentum", _b.load().mb_momentum(
-        _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"), _ptr(u, _TWO_BYTE, "u"), sh,
-        mu, _stream(stream)))
+    _same("momentum", grad, momentum)
+    _same("u", grad, u)
+    with _on(grad):
+        _b.check("mb_momentum", _b.load().mb_momentum(
+            _ptr(grad, _TWO_BYTE, "grad"), _ptr(momentum, (torch.float32,), "momentum"), _ptr(u, _TWO_BYTE, "u"), sh,
+            mu, _stream(stream)))
 
 
 def mb_newton_schulz_coeffs(u, v, coeffs, workspace=None, stream=None):
     """mb_newton_schulz with a per-step coefficient schedule: `coeffs` is a sequence of
     (a, b, c), one per step (its length is the number of steps)."""
-    import ctypes
     flat = [float(x) for abc in coeffs for x in abc]
     if len(flat) != 3 * len(coeffs):
         raise ValueError("coeffs must be a sequence of (a, b, c) triples")
     arr = (ctypes.c_float * max(len(flat), 1))(*flat)
     sh = _shape(u)
+    _same("v", u, v)
     ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols)), workspace, u.device)
-    _b.check("mb_newton_schulz_coeffs", _b.load().mb_newton_schulz_coeffs(
-        _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, len(coeffs), arr, ws.data_ptr(),
-        ws.numel() * ws.element_size(), _stream(stream)))
+    with _on(u):
+        _b.check("mb_newton_schulz_coeffs", _b.load().mb_newton_schulz_coeffs(
+            _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, len(coeffs), arr, ws.data_ptr(),
+            ws.numel() * ws.element_size(), _stream(stream)))
     return ws
 
 
 def mb_newton_schulz(u, v, ns_steps: int = 5, workspace=None, stream=None):
     sh = _shape(u)
+    _same("v", u, v)
     ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols)), workspace, u.device)
-    _b.check("mb_newton_schulz", _b.load().mb_newton_schulz(
-        _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, ns_steps, ws.data_ptr(),
-        ws.numel() * ws.element_size(), _stream(stream)))
+    with _on(u):
+        _b.check("mb_newton_schulz", _b.load().mb_newton_schulz(
+            _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, ns_steps, ws.data_ptr(),
+            ws.numel() * ws.element_size(), _stream(stream)))
     return ws
 
 
@@ -197,25 +247,34 @@ def mb_newton_schulz_noalloc(u, v, ns_steps: int = 5, stream=None):
     MB_NOALLOC_SCRATCH_BYTES); calls share it, so do not overlap them on the GPU.
     """
     sh = _shape(u)
-    _b.check("mb_newton_schulz_noalloc", _b.load().mb_newton_schulz_noalloc(
-        _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, ns_steps, _stream(stream)))
+    _same("v", u, v)
+    with _on(u):
+        _b.check("mb_newton_schulz_noalloc", _b.load().mb_newton_schulz_noalloc(
+            _ptr(u, _TWO_BYTE, "u"), _ptr(v, _TWO_BYTE, "v"), sh, ns_steps, _stream(stream)))
 
 
 def mb_update(bank, mantissa, v, lr: float, wd: float, stream=None):
     sh = _shape(bank)
-    _b.check("mb_update", _b.load().mb_update(
-        _ptr(bank, _TWO_BYTE, "bank"), _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(v, _TWO_BYTE, "v"), sh, lr, wd,
-        _stream(stream)))
+    _same("mantissa", bank, mantissa)
+    _same("v", bank, v)
+    with _on(bank):
+        _b.check("mb_update", _b.load().mb_update(
+            _ptr(bank, _TWO_BYTE, "bank"), _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(v, _TWO_BYTE, "v"), sh, lr,
+            wd, _stream(stream)))
 
 
 def mb_normuon_update(bank, mantissa, v, row_state, lr: float, wd: float, beta2: float = 0.95, workspace=None,
                       stream=None):
     sh = _shape(bank)
+    _same("mantissa", bank, mantissa)
+    _same("v", bank, v)
+    _same("row_state", bank, row_state, sh.batch * sh.rows)
     ws = _workspace(mb_workspace_bytes((sh.batch, sh.rows, sh.cols), True), workspace, bank.device)
-    _b.check("mb_normuon_update", _b.load().mb_normuon_update(
-        _ptr(bank, _TWO_BYTE, "bank"), _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(v, _TWO_BYTE, "v"),
-        _ptr(row_state, (torch.float32,), "row_state"), sh, lr, wd, beta2, ws.data_ptr(),
-        ws.numel() * ws.element_size(), _stream(stream)))
+    with _on(bank):
+        _b.check("mb_normuon_update", _b.load().mb_normuon_update(
+            _ptr(bank, _TWO_BYTE, "bank"), _ptr(mantissa, _TWO_BYTE, "mantissa"), _ptr(v, _TWO_BYTE, "v"),
+            _ptr(row_state, (torch.float32,), "row_state"), sh, lr, wd, beta2, ws.data_ptr(),
+            ws.numel() * ws.element_size(), _stream(stream)))
     return ws
 
 
