@@ -436,17 +436,11 @@ int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceS
         MB_TRY(encode_mn_map(&nb_.xmn2[t], k.ws + L.x[t], L.rows, L.batch, L.ld, 2));
         MB_TRY(encode_map(&nb_.st_x[t], k.ws + L.x[t], L.cols, L.rows, L.batch, L.ld, 32, 32,
                           CU_TENSOR_MAP_SWIZZLE_64B));
-        nb_.x[t] = k.at<uint16_t>(L.x[t]);
       }
       MB_TRY(encode_map(&nb_.ak, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 64, 128));
       MB_TRY(encode_map(&nb_.bk, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 64, 128));
       MB_TRY(encode_map(&nb_.st_a, k.ws + L.a, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       MB_TRY(encode_map(&nb_.st_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
-      nb_.a = k.at<uint16_t>(L.a);
-      nb_.x_ld = L.ld;
-      nb_.x_ms = static_cast<long long>(L.rows) * L.ld;
-      nb_.m_ld = L.ldm;
-      nb_.m_ms = static_cast<long long>(L.m) * L.ldm;
       nb_.scale = k.at<float>(L.scale);
       nb_.done = k.at<unsigned>(L.sync);
       nb_.batch = L.batch;

@@ -118,10 +118,7 @@ struct NsBank {
   CUtensorMap xk[3];                // X buffers, K-major boxes of 128 rows x 64
   CUtensorMap xmn2[3];              // X buffers, MN-major boxes of 64 K rows x 128 columns
   CUtensorMap ak, bk;               // A and B, K-major boxes of 128 rows x 64
-  CUtensorMap st_x[3], st_a, st_b;  // 32x32 store boxes (64-byte swizzle)
-  const uint16_t* x[3];             // X buffers (APPLY's epilogue input)
-  const uint16_t* a;                // A (POLY's epilogue input)
-  long long x_ld, x_ms, m_ld, m_ms;  // pitches (elements) and matrix strides
+  CUtensorMap st_x[3], st_a, st_b;  // 32x32 boxes (64-byte swizzle): the epilogues' stores, and their inputs
   const float* scale;               // per-matrix 1/(||u||_F + eps)
   unsigned* done;                   // completion counters [batch][MAX_NS_STEPS][3], zeroed before launch
   int batch, rows, cols, m, n, tall;

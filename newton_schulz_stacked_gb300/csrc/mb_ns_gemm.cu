@@ -233,25 +233,6 @@ __device__ __forceinline__ bool dependency(const Task& k, int& dit, int& dph) {
 
 // ---------------------------------------------------------------- epilogue
 
-// 16 consecutive bf16 of one row as 8 packed words (zeros outside [0, ncols) or a masked row).
-__device__ __forceinline__ void load_row16_raw(const uint16_t* base, long long ld, int row, int col0, int ncols,
-                                               bool row_ok, uint32_t (&w)[8]) {
-  if (row_ok && col0 + 16 <= ncols) {
-    const uint4* p = reinterpret_cast<const uint4*>(base + static_cast<long long>(row) * ld + col0);
-    const uint4 v0 = p[0], v1 = p[1];
-    w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-    w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t lo = 0, hi = 0;
-      if (row_ok && col0 + 2 * i < ncols) lo = base[static_cast<long long>(row) * ld + col0 + 2 * i];
-      if (row_ok && col0 + 2 * i + 1 < ncols) hi = base[static_cast<long long>(row) * ld + col0 + 2 * i + 1];
-      w[i] = lo | (hi << 16);
-    }
-  }
-}
-
 // Byte offset of 16-byte chunk `chunk` of row `row` in a [32][32] bf16 staging
 // buffer laid out as the TMA 64-byte swizzle expects (address bits [4,6) XOR
 // bits [7,9)): row-wise 16-byte writes of a warp then hit distinct banks.
@@ -264,11 +245,9 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return bf16_bits_to_float
 
 struct EpiJob {
   const CUtensorMap* st;   // store map of the output
-  long long ein_ld;        // row pitch of the matrix the epilogue input comes from
   // APPLY only: the first step also stores the bf16 residual of X_1 (st_lo), and the
-  // second step adds it back (ein_lo) so that its a*X_1 term uses X_1 to ~16 bits
+  // second step's input adds it back so that its a*X_1 term uses X_1 to ~16 bits
   const CUtensorMap* st_lo;
-  const uint16_t* ein_lo;
   int M, N, sym, mat, m0, n0, nt;
   int it;                  // Newton-Schulz step: picks its (a, b, c)
   float alpha;
@@ -297,14 +276,20 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 // the box hits distinct banks).  Boxes reaching past the matrix read zeros.
 struct InSrc {
   const CUtensorMap* map;
-  int row0, col0, mat, nch;
+  const CUtensorMap* map2;   // the second step of APPLY: X_1's residual, chunk for chunk after X
+  int row0, col0, mat, nch, nstr;
+  __device__ __forceinline__ int units() const { return nch * nstr; }
 };
 
 __device__ __forceinline__ InSrc input_of(const NsParams& P, const Task& tk, int row_base, int half) {
-  InSrc s{nullptr, 0, 0, 0, 0};
+  InSrc s{nullptr, nullptr, 0, 0, 0, 0, 1};
   if (tk.t < 0 || tk.ph == EPI_GRAM) return s;
   const NsBank& B = P.bank[tk.bi];
   s.map = tk.ph == EPI_POLY ? &B.st_a : &B.st_x[iterate_buffer(tk.it)];
+  if (tk.ph == EPI_APPLY && tk.it == 1) {
+    s.map2 = &B.st_x[2];
+    s.nstr = 2;
+  }
   s.row0 = tk.m0 + row_base;
   s.col0 = tk.n0 + half * (tk.nt >> 1);
   s.mat = tk.mat;
@@ -330,11 +315,14 @@ struct InFeed {
   int row_base, half;      // this warp's rows (CTA rank and quadrant) and column half
 };
 
-__device__ __forceinline__ void in_issue(InFeed& F, const InSrc& s, int c, int lane) {
+// Unit u of a task's input: chunk u / nstr of stream u % nstr (X, then X_1's residual).
+__device__ __forceinline__ void in_issue(InFeed& F, const InSrc& s, int u, int lane) {
   if (lane == 0) {
     const uint32_t slot = F.issued % IN_SLOTS;
+    const int c = s.nstr == 2 ? (u >> 1) : u;
+    const CUtensorMap* map = (s.nstr == 2 && (u & 1)) ? s.map2 : s.map;
     mbar_expect_tx(&F.full[slot], IN_BOX_BYTES);
-    tma_load_3d(F.buf + slot * IN_BOX_BYTES, s.map, &F.full[slot], s.col0 + 32 * c, s.row0, s.mat);
+    tma_load_3d(F.buf + slot * IN_BOX_BYTES, map, &F.full[slot], s.col0 + 32 * c, s.row0, s.mat);
   }
   ++F.issued;
 }
@@ -344,7 +332,7 @@ __device__ __forceinline__ void in_issue(InFeed& F, const InSrc& s, int c, int l
 // values before the warp got here).
 __device__ __forceinline__ void in_top_up(InFeed& F, const NsParams& P, int lane) {
   while (F.issued - F.used < static_cast<uint32_t>(IN_SLOTS)) {
-    if (F.cur_iss < F.cur.nch) {
+    if (F.cur_iss < F.cur.units()) {
       in_issue(F, F.cur, F.cur_iss++, lane);
       continue;
     }
@@ -360,7 +348,7 @@ __device__ __forceinline__ void in_top_up(InFeed& F, const NsParams& P, int lane
       // the scheduler acquired the task's inputs; order them before this thread's TMA reads
       if (lane == 0) fence_proxy_async_global();
     }
-    if (F.nxt_iss >= F.nxt.nch) return;
+    if (F.nxt_iss >= F.nxt.units()) return;
     in_issue(F, F.nxt, F.nxt_iss++, lane);
   }
 }
@@ -384,8 +372,6 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
   uint8_t* bufD = ebuf;          // [32 rows][32 cols] bf16, 64-byte swizzle
   uint8_t* bufT = ebuf + 2048;   // [32 cols][32 rows] bf16, 64-byte swizzle (or the residual)
   const int row0 = J.m0 + quad * 32;
-  const int row = row0 + lane;
-  const bool row_ok = row < J.M;
   const int I = J.m0 / BM;
   const int ncols = J.nt >> 1;
   const int cbeg = half * ncols;
@@ -394,8 +380,6 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
   const uint32_t word_off = 4u * ((lane >> 1) & 3);
   const float ca = P.ca[J.it], cb = P.cb[J.it], cc = P.cc[J.it];
 
-  uint32_t l_cur[8], l_nxt[8];
-  if (with_lo) load_row16_raw(J.ein_lo, J.ein_ld, row, J.n0 + cbeg, J.N, row_ok, l_cur);
 
   for (int c = 0; c < ncols; c += 32) {
     const int col0 = J.n0 + cbeg + c;
@@ -416,27 +400,48 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
     }
     const bool lo_out = EPI == EPI_APPLY && LO == LO_WRITE && direct;
 
-    const uint8_t* in = nullptr;
+    // this chunk's input row (and, in the second step's APPLY, X_1's residual), both halves,
+    // taken into registers at the chunk's start so that its slots refill under the chunk's work
+    uint32_t ex[16], lx[16];
     if (has_ein) {
       in_top_up(F, P, lane);
       const uint32_t slot = F.used % IN_SLOTS;
       if (!mbar_wait_or_abort(&F.full[slot], (F.used / IN_SLOTS) & 1, abort_flag)) return false;
-      in = F.buf + slot * IN_BOX_BYTES;
+      const uint8_t* in = F.buf + slot * IN_BOX_BYTES;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(in + sw64(lane, q));
+        ex[4 * q] = v.x; ex[4 * q + 1] = v.y; ex[4 * q + 2] = v.z; ex[4 * q + 3] = v.w;
+      }
+      uint32_t dep = 0;
+      if (with_lo) {
+        const uint32_t slot2 = (F.used + 1) % IN_SLOTS;
+        if (!mbar_wait_or_abort(&F.full[slot2], ((F.used + 1) / IN_SLOTS) & 1, abort_flag)) return false;
+        const uint8_t* inl = F.buf + slot2 * IN_BOX_BYTES;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = *reinterpret_cast<const uint4*>(inl + sw64(lane, q));
+          lx[4 * q] = v.x; lx[4 * q + 1] = v.y; lx[4 * q + 2] = v.z; lx[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dep ^= lx[i];
+      }
+      // the loads have landed in registers (an instruction reads them all) before the warp
+      // lets lane 0 overwrite their slots
+#pragma unroll
+      for (int i = 0; i < 16; ++i) dep ^= ex[i];
+      asm volatile("mov.b32 %0, %0;" : "+r"(dep));
+      F.used += with_lo ? 2 : 1;
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_smem();
+      in_top_up(F, P, lane);
     }
     if (lane == 0) bulk_wait_read_all();        // the previous chunk's stores have read the buffers
     __syncwarp();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int hc = col0 + 16 * h;
-      const bool more = c + 16 * h + 16 < ncols;
-      uint32_t e_cur[8];
-      if (has_ein) {
-        const uint4 v0 = *reinterpret_cast<const uint4*>(in + sw64(lane, 2 * h));
-        const uint4 v1 = *reinterpret_cast<const uint4*>(in + sw64(lane, 2 * h + 1));
-        e_cur[0] = v0.x; e_cur[1] = v0.y; e_cur[2] = v0.z; e_cur[3] = v0.w;
-        e_cur[4] = v1.x; e_cur[5] = v1.y; e_cur[6] = v1.z; e_cur[7] = v1.w;
-      }
-      if (with_lo && more) load_row16_raw(J.ein_lo, J.ein_ld, row, hc + 16, J.N, row_ok, l_nxt);
+      const uint32_t* e_cur = ex + 8 * h;
+      const uint32_t* l_cur = lx + 8 * h;
       uint32_t acc[16];
       tmem_ld_32x16(tacc + lane_base + static_cast<uint32_t>(cbeg + c + 16 * h), acc);
       tmem_ld_wait();
@@ -488,10 +493,6 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
         *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
         *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
       }
-      if (with_lo && more) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) l_cur[i] = l_nxt[i];
-      }
     }
     if (diag) {
       __syncwarp();
@@ -513,7 +514,6 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
         *reinterpret_cast<uint4*>(bufD + sw64(lane, j)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
       }
     }
-    if (has_ein) ++F.used;                      // its slot is refilled no earlier than the next top-up
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && (direct || mirror)) {
@@ -813,7 +813,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
       J.nt = tk.nt;
       J.alpha = 1.f;
       J.st_lo = nullptr;
-      J.ein_lo = nullptr;
       const uint32_t tacc = tmem + buf * ACC_COLS;
       bool ok;
       if (tk.ph == EPI_GRAM) {
@@ -822,30 +821,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
           J.alpha = sc * sc;
         }
         J.st = &B.st_a;
-        J.ein_ld = 0;
         J.M = J.N = B.m;
         J.sym = 1;
         ok = epilogue<EPI_GRAM, 0>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
       } else if (tk.ph == EPI_POLY) {
         J.st = &B.st_b;
-        J.ein_ld = B.m_ld;
         J.M = J.N = B.m;
         J.sym = 1;
         ok = epilogue<EPI_POLY, 0>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
       } else {
         if (tk.it == 0) J.alpha = B.scale[tk.mat];
         J.st = &B.st_x[iterate_buffer(tk.it + 1)];
-        J.ein_ld = B.x_ld;
         // X_1's residual waits in x[2], which the second APPLY overwrites tile by tile only
-        // after each tile has read its own part
+        // after each tile has read its own part (through the input ring, as input_of sets up
+        // for step 1)
         if (tk.it == 0 && P.steps > 1) J.st_lo = &B.st_x[2];
-        if (tk.it == 1) J.ein_lo = B.x[2] + tk.mat * B.x_ms;
         J.M = B.tall ? B.n : B.m;
         J.N = B.tall ? B.m : B.n;
         J.sym = 0;
         if (J.st_lo)
           ok = epilogue<EPI_APPLY, LO_WRITE>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
-        else if (J.ein_lo)
+        else if (tk.it == 1)
           ok = epilogue<EPI_APPLY, LO_READ>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
         else
           ok = epilogue<EPI_APPLY, 0>(P, J, tacc, quad, half, lane, ebuf, F, abort_flag);
