@@ -56,8 +56,10 @@
 //   warps 2..9    : epilogue of the CTA's own 128 rows, two warps per 32-lane
 //                   TMEM quadrant (each takes half the columns); task k's
 //                   epilogue runs under task k+1's MMAs; its input (A for POLY,
-//                   X for APPLY) arrives by TMA in 32x32 chunks a chunk ahead,
-//                   and its results leave through shared memory by TMA bulk stores
+//                   X for APPLY, plus X_1's residual in the second step) arrives
+//                   by TMA in 32x32 boxes through a two-slot ring refilled as each
+//                   chunk is taken, and its results leave through shared memory by
+//                   TMA bulk stores
 #include <atomic>
 
 #include "mb_device.cuh"
@@ -297,8 +299,9 @@ __device__ __forceinline__ InSrc input_of(const NsParams& P, const Task& tk, int
   return s;
 }
 
-// One epilogue warp's input ring: IN_SLOTS shared buffers that TMA fills up to
-// IN_SLOTS - 1 chunks ahead of their use.  Once a task's chunks are all issued, the ring
+// One epilogue warp's input ring: IN_SLOTS shared buffers of one 32x32 box (a unit) each,
+// refilled by TMA as soon as the epilogue has taken a chunk's units into registers, so the
+// next units load under the chunk's work.  Once a task's units are all issued, the ring
 // runs on into the next task's as soon as that task's record is published (a
 // non-blocking test: the next task may depend on this one).  The counters are
 // warp-uniform; lane 0 issues.
@@ -308,9 +311,9 @@ struct InFeed {
   const Task* rec;         // the task records ...
   uint64_t* slot_full;     // ... and their barriers
   uint32_t k;              // the task this warp is working on
-  uint32_t issued, used;   // chunks issued and consumed so far
+  uint32_t issued, used;   // units issued and consumed so far
   InSrc cur, nxt;          // the inputs of task k and task k + 1
-  int cur_iss, nxt_iss;    // how many of their chunks are issued
+  int cur_iss, nxt_iss;    // how many of their units are issued
   bool nxt_known;
   int row_base, half;      // this warp's rows (CTA rank and quadrant) and column half
 };
@@ -327,9 +330,9 @@ __device__ __forceinline__ void in_issue(InFeed& F, const InSrc& s, int u, int l
   ++F.issued;
 }
 
-// Issues input chunks while the ring has room: the rest of task k's, then task k + 1's.
-// A slot is refilled only after the chunk it held was consumed (every lane used the
-// values before the warp got here).
+// Issues input units while the ring has room: the rest of task k's, then task k + 1's.
+// A slot is refilled only after the unit it held was consumed: every lane's loads of it
+// have landed in registers (an instruction has read them) before the warp got here.
 __device__ __forceinline__ void in_top_up(InFeed& F, const NsParams& P, int lane) {
   while (F.issued - F.used < static_cast<uint32_t>(IN_SLOTS)) {
     if (F.cur_iss < F.cur.units()) {
