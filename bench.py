@@ -369,8 +369,9 @@ def run_native(args):
         # End to end through the public call: every step uploads its gradients from pinned host
         # memory and brings the updated bf16 weights back to pinned host memory.  The copies run
         # on two copy streams beside the compute: step k+1's gradients upload while step k runs
-        # (double-buffered device gradients), and step k's weights are snapshotted on the device
-        # and downloaded while step k+1 runs.
+        # (double-buffered device gradients), and step k's update also writes the new weights into
+        # a second device buffer (the banks' bank_copy, double-buffered), downloaded while step
+        # k+1 runs.
         main_s = torch.cuda.current_stream()
         h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         gdev = [[torch.empty_like(b.bank) for b in banks] for _ in range(2)]
@@ -397,15 +398,14 @@ def run_native(args):
                 if k + 1 < n:
                     upload(k + 1)
                 main_s.wait_event(ev_h2d[b_])
-                for bank, g in zip(banks, gdev[b_]):
+                if k >= 2:
+                    main_s.wait_event(ev_d2h[b_])   # step k-2's weights have left snap[b_]
+                for bank, g, sn in zip(banks, gdev[b_], snap[b_]):
                     bank.grad = g
+                    bank.bank_copy = sn
                 nss.muon_multi_step(banks, wl.lr, wl.wd, wl.mu, normuon=wl.normuon, beta2=wl.beta2,
                                     ns_steps=wl.ns_steps, workspace=ws)
                 ev_gfree[b_].record(main_s)
-                if k >= 2:
-                    main_s.wait_event(ev_d2h[b_])
-                for sn, bank in zip(snap[b_], banks):
-                    sn.copy_(bank.bank, non_blocking=True)
                 ev_snap[b_].record(main_s)
                 with torch.cuda.stream(d2h_s):
                     d2h_s.wait_event(ev_snap[b_])
@@ -425,11 +425,14 @@ def run_native(args):
         e2e_run(k_e2e)
         e1.record(main_s)
         torch.cuda.synchronize()
+        for bank in banks:
+            bank.bank_copy = None
         e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3), dev)
         e2e = {"value": job_rate(world, k_e2e, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k_e2e,
-               "what": "pinned host gradients -> device, muon_multi_step, updated bf16 weights -> pinned host; "
-                       "copies on two copy streams overlap the neighbouring steps' compute"}
+               "what": "pinned host gradients -> device, muon_multi_step (its update also writes the new bf16 "
+                       "weights to a second device buffer), that buffer -> pinned host; copies on two copy "
+                       "streams overlap the neighbouring steps' compute"}
 
     if rank == 0:
         line = {

@@ -90,6 +90,10 @@ typedef struct {
   uint16_t* mantissa;    /* uint16 [batch, rows, cols], updated in place */
   float* row_state;      /* fp32 [batch, rows] NorMuon second moment; NULL unless normuon */
   mb_shape shape;
+  void* bank_copy;       /* optional bf16 [batch, rows, cols]: the update also writes the new bank
+                            here (for example for a download that overlaps the next step);
+                            NULL: not written.  16-byte aligned, must not overlap any other
+                            buffer of the call. */
 } mb_bank_desc;
 
 #define MB_MAX_BANKS 8

@@ -132,13 +132,19 @@ def normuon_bank_step(bank, grad, momentum, mantissa, row_state, lr: float, wd: 
 
 
 class BankState:
-    """The caller-owned tensors of one bank: bank, grad, momentum, mantissa (and row_state)."""
+    """The caller-owned tensors of one bank: bank, grad, momentum, mantissa (and row_state).
 
-    def __init__(self, bank, grad, momentum, mantissa, row_state=None):
+    bank_copy, when set, is a second bf16 tensor of the bank's shape that each step's update
+    also writes the new bank into (for example a buffer to download while the next step runs).
+    """
+
+    def __init__(self, bank, grad, momentum, mantissa, row_state=None, bank_copy=None):
         self.bank, self.grad, self.momentum, self.mantissa, self.row_state = bank, grad, momentum, mantissa, row_state
+        self.bank_copy = bank_copy
 
     def desc(self) -> _b.MbBankDesc:
-        for name, t in (("grad", self.grad), ("momentum", self.momentum), ("mantissa", self.mantissa)):
+        for name, t in (("grad", self.grad), ("momentum", self.momentum), ("mantissa", self.mantissa),
+                        ("bank_copy", self.bank_copy)):
             _same(name, self.bank, t)
         if self.row_state is not None:
             sh = _shape(self.bank)
@@ -146,7 +152,8 @@ class BankState:
         return _b.MbBankDesc(_ptr(self.bank, _TWO_BYTE, "bank"), _ptr(self.grad, _TWO_BYTE, "grad"),
                              _ptr(self.momentum, (torch.float32,), "momentum"),
                              _ptr(self.mantissa, _TWO_BYTE, "mantissa"),
-                             _ptr(self.row_state, (torch.float32,), "row_state"), _shape(self.bank))
+                             _ptr(self.row_state, (torch.float32,), "row_state"), _shape(self.bank),
+                             _ptr(self.bank_copy, _TWO_BYTE, "bank_copy"))
 
 
 def _descs(banks: Sequence[BankState]):

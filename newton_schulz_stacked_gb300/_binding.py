@@ -38,7 +38,7 @@ class MbShape(ctypes.Structure):
 
 class MbBankDesc(ctypes.Structure):
     _fields_ = [("bank", c_void_p), ("grad", c_void_p), ("momentum", c_void_p), ("mantissa", c_void_p),
-                ("row_state", c_void_p), ("shape", MbShape)]
+                ("row_state", c_void_p), ("shape", MbShape), ("bank_copy", c_void_p)]
 
 
 _P = c_void_p

@@ -219,6 +219,7 @@ int final_buffer(int ns_steps) { return ns_steps == 0 ? 1 : iterate_buffer(ns_st
 
 struct Bank {
   uint16_t* bank;
+  uint16_t* bank_copy;  // optional second destination of the updated bank
   const uint16_t* grad;
   float* mom;
   uint16_t* mant;
@@ -519,6 +520,7 @@ int stage_k3(const Bank* b, int nb, bool normuon, float lr, float wd, const uint
              cudaStream_t st, bool dev_scalars = false) {
   EwParams p = ew_params(b, nb, [&](const Bank& k, EwBank& e) {
     e.bank = k.bank;
+    e.bank_copy = k.bank_copy;
     e.mant = k.mant;
     e.rowscale = normuon ? k.at<float>(k.L.rowscale) : nullptr;
     const double lrd = lr, wdd = wd;
@@ -543,6 +545,7 @@ int validate_bank(const mb_bank_desc& d, int normuon) {
   MB_TRY(check_ptr(d.momentum));
   MB_TRY(check_ptr(d.mantissa));
   if (normuon) MB_TRY(check_ptr(d.row_state));
+  if (d.bank_copy && !aligned16(d.bank_copy)) return MB_ERR_ALIGN;
   return MB_OK;
 }
 
@@ -586,6 +589,7 @@ int run_step(const mb_bank_desc* d, int nb, float lr, float wd, float mu, int no
   int vld[MAX_BANKS];
   for (int i = 0; i < nb; ++i) {
     b[i].bank = static_cast<uint16_t*>(d[i].bank);
+    b[i].bank_copy = static_cast<uint16_t*>(d[i].bank_copy);
     b[i].grad = static_cast<const uint16_t*>(d[i].grad);
     b[i].mom = d[i].momentum;
     b[i].mant = d[i].mantissa;
@@ -695,14 +699,14 @@ int mb_multi_workspace_bytes(const mb_bank_desc* banks, int n_banks, int normuon
 int muon_bank_step(void* bank_bf16, const void* grad_bf16, float* momentum_f32, uint16_t* mantissa,
                    mb_shape shape, float lr, float wd, float mu, int ns_steps, void* workspace,
                    size_t workspace_bytes, void* cuda_stream) {
-  mb_bank_desc d{bank_bf16, grad_bf16, momentum_f32, mantissa, nullptr, shape};
+  mb_bank_desc d{bank_bf16, grad_bf16, momentum_f32, mantissa, nullptr, shape, nullptr};
   return run_step(&d, 1, lr, wd, mu, 0, 0.f, ns_steps, workspace, workspace_bytes, cuda_stream);
 }
 
 int normuon_bank_step(void* bank_bf16, const void* grad_bf16, float* momentum_f32, uint16_t* mantissa,
                       float* row_state_f32, mb_shape shape, float lr, float wd, float mu, float beta2,
                       int ns_steps, void* workspace, size_t workspace_bytes, void* cuda_stream) {
-  mb_bank_desc d{bank_bf16, grad_bf16, momentum_f32, mantissa, row_state_f32, shape};
+  mb_bank_desc d{bank_bf16, grad_bf16, momentum_f32, mantissa, row_state_f32, shape, nullptr};
   return run_step(&d, 1, lr, wd, mu, 1, beta2, ns_steps, workspace, workspace_bytes, cuda_stream);
 }
 

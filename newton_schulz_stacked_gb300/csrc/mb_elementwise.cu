@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(EW_THREADS) k3_kernel(const __grid_constant__ 
   const size_t moff = static_cast<size_t>(mat) * E;
   uint16_t* wb = B.bank + moff;
   uint16_t* mb_ = B.mant + moff;
+  uint16_t* wc = B.bank_copy ? B.bank_copy + moff : nullptr;
   const uint16_t* v = B.xin + static_cast<size_t>(mat) * B.rows * B.ld;
   const float* rs = NORMUON ? B.rowscale + static_cast<size_t>(mat) * B.rows : nullptr;
   const float decay = B.dscal ? B.dscal[DSCAL_DECAY] : B.decay;
@@ -395,6 +396,7 @@ __global__ void __launch_bounds__(EW_THREADS) k3_kernel(const __grid_constant__ 
       }
       *reinterpret_cast<uint4*>(wb + e) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4*>(mb_ + e) = make_uint4(m[0], m[1], m[2], m[3]);
+      if (wc) *reinterpret_cast<uint4*>(wc + e) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
     for (int e = e0 + threadIdx.x; e < e1; e += EW_THREADS) {
@@ -405,6 +407,7 @@ __global__ void __launch_bounds__(EW_THREADS) k3_kernel(const __grid_constant__ 
       update_one(w, m, vf, decay, neg_lr);
       wb[e] = static_cast<uint16_t>(w);
       mb_[e] = static_cast<uint16_t>(m);
+      if (wc) wc[e] = static_cast<uint16_t>(w);
     }
   }
 }

@@ -23,6 +23,7 @@ struct EwBank {
   float* mom;              // K1 momentum (null in pack mode)
   uint16_t* bank;          // K3 weight bf16 bits
   uint16_t* mant;          // K3 mantissa
+  uint16_t* bank_copy;     // K3: optional second destination of the updated bf16 bank (null: none)
   uint16_t* xout;          // K1: u destination (pitch ld); ns0/unpack: destination
   const uint16_t* xin;     // K3/ns0/unpack: source (pitch ld)
   const float* rowscale;   // K3 NorMuon per-row factor (null otherwise)

@@ -126,6 +126,10 @@ def test_multi_step_argument_errors(lib):
     assert lib.muon_multi_step(None, 1, 0.02, 0.01, 0.95, 0, 0.95, 5, good, 1 << 30, None) == b.MB_ERR_NULL
     # normuon over banks without row state
     assert lib.muon_multi_step(arr, 2, 0.02, 0.01, 0.95, 1, 0.95, 5, good, 1 << 30, None) == b.MB_ERR_NULL
+    # the optional copy of the updated bank must be 16-byte aligned
+    arr[1].bank_copy = good + 2
+    assert lib.muon_multi_step(arr, 2, 0.02, 0.01, 0.95, 0, 0.95, 5, good, 1 << 30, None) == b.MB_ERR_ALIGN
+    arr[1].bank_copy = None
     # device-memory hyperparameters: the buffer pointer is checked before anything else
     assert lib.muon_multi_step_dev(arr, 2, None, 0, 5, good, 1 << 30, None) == b.MB_ERR_NULL
     assert lib.muon_multi_step_dev(arr, 2, good + 4, 0, 5, good, 1 << 30, None) == b.MB_ERR_ALIGN

@@ -259,6 +259,27 @@ def test_multi_step_equals_single_steps(nss):
         np.testing.assert_array_equal(f32(a.momentum), f32(b.momentum))
 
 
+@pytest.mark.parametrize("normuon", [False, True])
+def test_bank_copy_receives_the_updated_bank(nss, normuon):
+    """A bank's optional copy gets exactly the updated bank, on both update paths (columns a
+    multiple of 8 and not), and the step is otherwise the same as without it."""
+    shapes = [(4, 256, 384), (3, 200, 328), (10, 6, 12), (2, 7, 9)]
+    states = [_case(60 + i, s) for i, s in enumerate(shapes)]
+    with_copy, plain = [], []
+    for (w, mant, mom, row, g) in states:
+        rt = to_dev(row) if normuon else None
+        with_copy.append(nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant), rt, torch.zeros_like(to_dev(w))))
+        plain.append(nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant), rt.clone() if normuon else None))
+    nss.muon_multi_step(with_copy, LR, WD, MU, normuon=normuon, ns_steps=5)
+    nss.muon_multi_step(plain, LR, WD, MU, normuon=normuon, ns_steps=5)
+    torch.cuda.synchronize()
+    assert nss.mb_sync_status() == 0
+    for a, b in zip(with_copy, plain):
+        np.testing.assert_array_equal(u16(a.bank_copy), u16(a.bank))
+        np.testing.assert_array_equal(u16(a.bank), u16(b.bank))
+        np.testing.assert_array_equal(u16(a.mantissa), u16(b.mantissa))
+
+
 def test_step_on_a_caller_stream(nss):
     """The step is ordered on the stream it is given, including the fp32 gate banks that run on the
     library's side stream (forked from and joined back to the caller's stream)."""
