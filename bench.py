@@ -205,20 +205,35 @@ def cpu_oracle_sample(wl, per_bank, seed_step=1):
     return total_est, sampled, ", ".join(desc)
 
 
-def cores():
+def host_cores():
     try:
         return len(os.sched_getaffinity(0))
     except AttributeError:
-        return os.cpu_count()
+        return os.cpu_count() or 1
+
+
+def cores():
+    """The host threads the fp64 oracle can use: the affinity set, capped by a BLAS thread limit."""
+    n = host_cores()
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            n = min(n, int(v))
+    return n
 
 
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
-    import synth
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and os.environ.get("OMP_NUM_THREADS") == "1":
+        # torchrun gives every rank one BLAS thread by default; rank 0 alone runs this arm, so it
+        # takes the host's cores as a single-process run would (set before NumPy loads its BLAS)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = str(host_cores())
+    import synth
     wl = synth.WORKLOADS[args.workload]
     sample = {"attn": 1, "mlp": 1, "smear_gate": 1, "attn_gate": 10}
     for _ in range(args.warmup):

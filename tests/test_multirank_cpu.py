@@ -65,3 +65,26 @@ def test_single_process_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_rate(1, 100, 250.0) == pytest.approx(400.0)
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
+    """Under torchrun rank 0 alone times the oracle (with the host's cores, not the one BLAS
+    thread torchrun gives each rank), prints one JSON line, and every rank exits 0."""
+    import json
+    import subprocess
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    try:
+        host = len(os.sched_getaffinity(0))
+    except AttributeError:
+        host = os.cpu_count()
+    assert d["cpu_baseline"]["cores"] == host
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
