@@ -259,6 +259,25 @@ def test_multi_step_equals_single_steps(nss):
         np.testing.assert_array_equal(f32(a.momentum), f32(b.momentum))
 
 
+def test_more_large_banks_than_one_fused_launch_takes(nss):
+    """Six large banks in one call run as two fused Newton-Schulz launches (four banks each at
+    most), each with its own task counter; the result is bit-identical to six single-bank steps."""
+    shapes = [(3, 256, 384), (2, 384, 256), (4, 200, 328), (1, 768, 768), (2, 128, 640), (3, 300, 520)]
+    states = [_case(80 + i, s) for i, s in enumerate(shapes)]
+    multi = [nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant)) for (w, mant, mom, row, g) in states]
+    single = [nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant)) for (w, mant, mom, row, g) in states]
+    for _ in range(2):
+        nss.muon_multi_step(multi, LR, WD, MU, ns_steps=5)
+        for b in single:
+            nss.muon_bank_step(b.bank, b.grad, b.momentum, b.mantissa, LR, WD, MU, 5)
+    torch.cuda.synchronize()
+    assert nss.mb_sync_status() == 0
+    for a, b in zip(multi, single):
+        np.testing.assert_array_equal(u16(a.bank), u16(b.bank))
+        np.testing.assert_array_equal(u16(a.mantissa), u16(b.mantissa))
+        np.testing.assert_array_equal(f32(a.momentum), f32(b.momentum))
+
+
 @pytest.mark.parametrize("normuon", [False, True])
 def test_bank_copy_receives_the_updated_bank(nss, normuon):
     """A bank's optional copy gets exactly the updated bank, on both update paths (columns a
