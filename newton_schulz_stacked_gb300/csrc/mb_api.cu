@@ -28,6 +28,9 @@ struct Timing {
   int cap = 0, used = 0;
   std::vector<cudaEvent_t> ev;
   std::vector<int> label;
+  ~Timing() {   // a thread that ends between mb_timing_begin and mb_timing_end
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
 };
 thread_local Timing g_timing;
 
@@ -84,6 +87,12 @@ DeviceState g_dev[64];
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  // released when the host thread ends; work already queued on the stream still completes
+  ~SideStream() {
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (stream) cudaStreamDestroy(stream);
+  }
 };
 thread_local SideStream t_side[64];
 
