@@ -64,7 +64,7 @@ extern "C" {
 enum {
   MB_OK = 0,
   MB_ERR_NULL = -1,          /* a required pointer is NULL */
-  MB_ERR_SHAPE = -2,         /* batch/rows/cols <= 0, or an element count that overflows */
+  MB_ERR_SHAPE = -2,         /* batch/rows/cols <= 0, or a size past the limits of mb_shape */
   MB_ERR_ALIGN = -3,         /* a pointer is not 16-byte aligned */
   MB_ERR_NS_STEPS = -4,      /* ns_steps outside 0..16 */
   MB_ERR_WORKSPACE = -5,     /* workspace NULL or smaller than required */
@@ -77,7 +77,10 @@ enum {
   MB_ERR_DEVICE = -12        /* a device-side consistency check failed (from mb_sync_status) */
 };
 
-/* One bank: `batch` matrices of rows x cols. */
+/* One bank: `batch` matrices of rows x cols.  Limits (else MB_ERR_SHAPE): rows x cols
+ * <= 2^30 elements per matrix, batch x rows x cols <= 2^40, batch x rows <= 2^30, and
+ * batch x ceil(rows x cols / 8192) <= 2^30; the banks of one multi-bank call together
+ * hold at most 2^30 matrices, 2^30 rows and 2^30 such 8192-element blocks. */
 typedef struct {
   int32_t batch, rows, cols;
 } mb_shape;

@@ -558,12 +558,25 @@ int validate_bank(const mb_bank_desc& d, int normuon) {
   return MB_OK;
 }
 
+// The banks of one call share each launch, whose grid and per-launch counts of
+// matrices and rows are 32-bit: together they stay within what one bank may hold.
+int check_totals(const Layout* L, int nb) {
+  long long blocks = 0, mats = 0, rows = 0;
+  for (int i = 0; i < nb; ++i) {
+    blocks += static_cast<long long>(L[i].batch) * L[i].P;
+    mats += L[i].batch;
+    rows += static_cast<long long>(L[i].batch) * L[i].rows;
+  }
+  return (blocks > (1ll << 30) || mats > (1ll << 30) || rows > (1ll << 30)) ? MB_ERR_SHAPE : MB_OK;
+}
+
 int workspace_for(const mb_bank_desc* d, int nb, int normuon, Layout* L, size_t* total) {
   size_t off = 0;
   for (int i = 0; i < nb; ++i) {
     L[i] = make_layout(d[i].shape, normuon, off);
     off = L[i].end;
   }
+  MB_TRY(check_totals(L, nb));
   *total = off;
   return MB_OK;
 }

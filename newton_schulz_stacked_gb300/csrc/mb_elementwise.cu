@@ -453,9 +453,9 @@ cudaError_t launch_unpack(const EwParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int small_ns_smem_bytes(int rows, int cols) {
-  const int m = rows < cols ? rows : cols;
-  return (2 * rows * cols + 2 * m * m) * static_cast<int>(sizeof(float));
+long long small_ns_smem_bytes(int rows, int cols) {
+  const long long m = rows < cols ? rows : cols;
+  return (2ll * rows * cols + 2 * m * m) * static_cast<long long>(sizeof(float));
 }
 
 cudaError_t launch_small_ns(const SmallParams& p, bool in_smem, cudaStream_t s) {
@@ -475,12 +475,13 @@ cudaError_t launch_small_ns(const SmallParams& p, bool in_smem, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     attr_done[dev].store(true, std::memory_order_release);
   }
-  int bytes = 0;
+  long long bytes = 0;
   for (int i = 0; i < p.nb; ++i) {
-    const int b = small_ns_smem_bytes(p.b[i].rows, p.b[i].cols);
+    const long long b = small_ns_smem_bytes(p.b[i].rows, p.b[i].cols);
     bytes = b > bytes ? b : bytes;
   }
-  small_ns_kernel<true><<<p.total_blocks, SMALL_THREADS, bytes, s>>>(p);
+  if (bytes > SMALL_SMEM_MAX) return cudaErrorInvalidValue;   // such banks take the other path
+  small_ns_kernel<true><<<p.total_blocks, SMALL_THREADS, static_cast<size_t>(bytes), s>>>(p);
   return cudaGetLastError();
 }
 

@@ -149,7 +149,7 @@ cudaError_t launch_unpack(const EwParams& p, cudaStream_t s);
 // Shared memory the in-shared-memory fp32 NS needs for one rows x cols matrix;
 // banks up to SMALL_SMEM_MAX use it, larger ones run through the workspace.
 constexpr int SMALL_SMEM_MAX = 200 * 1024;
-int small_ns_smem_bytes(int rows, int cols);
+long long small_ns_smem_bytes(int rows, int cols);
 cudaError_t launch_small_ns(const SmallParams& p, bool in_smem, cudaStream_t s);
 cudaError_t launch_row_sumsq(const RowParams& p, cudaStream_t s);
 cudaError_t launch_row_scale(const RowParams& p, cudaStream_t s);

@@ -66,11 +66,39 @@ def test_workspace_bytes(lib):
     assert st == 0 and n_small >= 2 * 10 * 6 * 16 * 2 + 2 * 10 * 72 * 4
 
 
-@pytest.mark.parametrize("shape", [(0, 4, 4), (1, 0, 4), (1, 4, -1), (1, 1 << 16, 1 << 16)])
+@pytest.mark.parametrize("shape", [(0, 4, 4), (1, 0, 4), (1, 4, -1), (1, 1 << 16, 1 << 16),
+                                   (1, (1 << 15) + 1, 1 << 15),          # one element past 2^30 per matrix
+                                   ((1 << 30) + 1, 1, 1),                # 2^30 rows (and matrices) per bank
+                                   (1 << 11, 1 << 15, 1 << 15)])         # 2^41 elements in one bank
 def test_workspace_rejects_bad_shapes(lib, shape):
     from newton_schulz_stacked_gb300 import _binding as b
     st, _ = _ws(lib, shape)
     assert st == b.MB_ERR_SHAPE
+
+
+@pytest.mark.parametrize("shape", [(1, 1 << 15, 1 << 15), (1 << 30, 1, 1), (1 << 10, 1 << 15, 1 << 15)])
+def test_workspace_accepts_the_largest_shapes(lib, shape):
+    st, n = _ws(lib, shape)
+    assert st == 0 and n >= 3 * shape[0] * shape[1] * shape[2] * 2
+
+
+def test_banks_of_one_call_share_the_launch_limits(lib):
+    """Each of these banks is legal alone; two of them overflow the 32-bit grid and the counts of
+    matrices and rows that the launches of one call share, so the call refuses them."""
+    from newton_schulz_stacked_gb300 import _binding as b
+    good = 1 << 12
+    arr = (b.MbBankDesc * 2)()
+    for i in range(2):
+        arr[i] = b.MbBankDesc(good, good, good, good, None, b.shape_of(1 << 30, 1, 1))
+    out = ctypes.c_size_t()
+    assert lib.mb_multi_workspace_bytes(arr, 1, 0, ctypes.byref(out)) == 0
+    assert lib.mb_multi_workspace_bytes(arr, 2, 0, ctypes.byref(out)) == b.MB_ERR_SHAPE
+    assert lib.muon_multi_step(arr, 2, 0.02, 0.01, 0.95, 0, 0.95, 5, good, 1 << 62, None) == b.MB_ERR_SHAPE
+    assert lib.muon_multi_step_dev(arr, 2, good, 0, 5, good, 1 << 62, None) == b.MB_ERR_SHAPE
+    # half as many matrices each: together exactly at the limit
+    for i in range(2):
+        arr[i].shape = b.shape_of(1 << 29, 1, 1)
+    assert lib.mb_multi_workspace_bytes(arr, 2, 0, ctypes.byref(out)) == 0
 
 
 def test_workspace_views(lib):
