@@ -48,6 +48,25 @@ def test_momentum(nss, shape):
         assert np.all(np.abs(u_gpu[k] - u_exact) <= u_bound(u_exact, g[k], b_ref))
 
 
+# the ends of the momentum range: mu = 0 keeps only the gradient, mu = 1 only the buffer
+@pytest.mark.parametrize("mu", [0.0, 0.5, 1.0])
+def test_momentum_edge_coefficients(nss, mu):
+    shape = (3, 200, 328)
+    w, mant, mom, _, g = _case(16, shape, std=1.0)
+    mom = np.random.default_rng(17).standard_normal(shape).astype(np.float32)
+    gt, mt = to_dev(g), to_dev(mom)
+    ut = torch.empty_like(gt)
+    nss.mb_momentum(gt, mt, ut, mu)
+    torch.cuda.synchronize()
+    b_gpu, u_gpu = f32(mt), O.bf16_bits_to_f64(u16(ut))
+    for k in range(shape[0]):
+        b_ref, _, u_exact = O.momentum(g[k], mom[k], mu)
+        assert O.rel_frobenius(b_gpu[k], b_ref) <= MOMENTUM_TOL
+        assert np.all(np.abs(u_gpu[k] - u_exact) <= u_bound(u_exact, g[k], b_ref))
+    if mu == 1.0:
+        np.testing.assert_array_equal(b_gpu, mom)      # nothing of the gradient enters the buffer
+
+
 # ---------------------------------------------------------------- S5
 
 @pytest.mark.parametrize("shape", [(4, 128, 128), (3, 200, 328), (2, 6, 12), (2, 3072, 768), (1, 7, 9)])
@@ -224,18 +243,19 @@ def test_normuon_step(nss, shape):
     assert check_update(w, mant, v_gpu, u16(t["w"]), u16(t["m"]), LR, WD, R, C, vhat=vhat) <= UPDATE_TOL
 
 
-def test_normuon_update_stage(nss):
+@pytest.mark.parametrize("beta2", [0.9, 0.0, 1.0])
+def test_normuon_update_stage(nss, beta2):
     shape = (3, 300, 136)
     w, mant, _, row, _ = _case(24, shape)
     row = np.random.default_rng(25).uniform(0, 1e-3, row.shape).astype(np.float32)
     v = synth.v_bits(26, *shape, scale=0.05)
     v[1, 7] = 0   # a zero row
     wt, mt, rt = to_dev(w), to_dev(mant), to_dev(row)
-    nss.mb_normuon_update(wt, mt, to_dev(v), rt, LR, WD, 0.9)
+    nss.mb_normuon_update(wt, mt, to_dev(v), rt, LR, WD, beta2)
     torch.cuda.synchronize()
     vhat = []
     for k in range(3):
-        vh, s = O.normuon(O.bf16_bits_to_f64(v[k]), row[k], 0.9)
+        vh, s = O.normuon(O.bf16_bits_to_f64(v[k]), row[k], beta2)
         assert O.rel_frobenius(f32(rt)[k], s) <= STATE_TOL
         vhat.append(vh)
     assert check_update(w, mant, v, u16(wt), u16(mt), LR, WD, shape[1], shape[2], vhat=vhat) <= UPDATE_TOL
