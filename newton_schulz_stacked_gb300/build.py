@@ -23,6 +23,11 @@ LIB_PATH = os.path.join(HERE, "libmuonbank.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--diag-suppress", "177"]
+# the compiler's NVVM stage (cicc) on the aarch64 hosts sometimes dies with a segmentation
+# fault on the tensor-core source (about one compile in six to one in three, on the same
+# inputs; not its stack: on x86 the file compiles within a 1 MiB stack); a crashed file is
+# compiled again on its own, up to this many attempts in all (all failing: ~5e-5 at 1 in 3)
+COMPILE_ATTEMPTS = 9
 
 
 def _nvcc() -> str:
@@ -60,10 +65,7 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         results = list(ex.map(compile_one, zip(srcs, objs)))
     for i, (cmd, r) in enumerate(results):
-        # the compiler's NVVM stage (cicc) on the aarch64 hosts sometimes dies with a
-        # segmentation fault on this source (about one compile in six to one in three, on the
-        # same inputs); a crashed file is retried on its own before the build gives up
-        for _ in range(4):
+        for _ in range(COMPILE_ATTEMPTS - 1):
             if r.returncode == 0:
                 break
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr + "retrying this file alone\n")

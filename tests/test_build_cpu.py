@@ -55,6 +55,6 @@ def test_a_file_that_always_crashes_fails_the_build(sandbox, monkeypatch):
     monkeypatch.setattr(B, "subprocess", _fake_compiler({"mb_ns_gemm.cu": 99}, calls))
     with pytest.raises(RuntimeError, match="mb_ns_gemm.cu"):
         B.build_library(force=True)
-    assert calls.count("mb_ns_gemm.cu") == 5            # the parallel attempt and four retries
+    assert calls.count("mb_ns_gemm.cu") == B.COMPILE_ATTEMPTS == 9   # the parallel attempt and eight retries
     assert "link" not in calls
     assert not os.path.exists(B.LIB_PATH)
