@@ -192,6 +192,11 @@ __device__ __forceinline__ Operands task_operands(const NsBank& B, const Task& k
   return o;
 }
 
+// In a 256-wide tile on the diagonal of a symmetric phase (A = X X^T or X^T X, and A A with
+// A symmetric), each CTA's half of the B operand holds the same rows, in the same layout, as
+// its A tile: the producer loads only A and the MMAs read B from there.
+__device__ __forceinline__ bool b_is_a(const Task& k) { return k.ph != EPI_APPLY && k.m0 == k.n0 && k.nt == 256; }
+
 // ---------------------------------------------------------------- cross-CTA completion
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -691,6 +696,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         const int KB = (op.K + BK - 1) / BK;
         const int m0 = tk.m0 + static_cast<int>(rank) * BM;         // this CTA's A rows
         const int nb0 = tk.n0 + static_cast<int>(rank) * (tk.nt >> 1);   // this CTA's B rows
+        const bool load_b = !b_is_a(tk);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           if (it >= STAGES && !mbar_wait_cluster_or_abort(&empty[st], ph ^ 1u, abort_flag)) {
@@ -698,15 +704,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
             ok = false;
             break;
           }
-          if (even) mbar_expect_tx(&full[st], 2u * STAGE_BYTES);   // both CTAs' boxes
+          if (even) mbar_expect_tx(&full[st], load_b ? 2u * STAGE_BYTES : 2u * A_TILE_BYTES);   // both CTAs' boxes
           const uint32_t fb = full_even + 8u * static_cast<uint32_t>(st);
           uint8_t* a = sA + st * A_TILE_BYTES;
           uint8_t* b = sB + st * BH_TILE_BYTES;
           const int k0 = kb * BK;
           if (!op.a_mn) tma_load_3d_pair(a, op.a, fb, k0, m0, tk.mat);
           else tma_load_4d_pair(a, op.a, fb, 0, k0, m0 >> 6, tk.mat);
-          if (!op.b_mn) tma_load_3d_pair(b, op.b, fb, k0, nb0, tk.mat);
-          else tma_load_4d_pair(b, op.b, fb, 0, k0, nb0 >> 6, tk.mat);
+          if (load_b) {
+            if (!op.b_mn) tma_load_3d_pair(b, op.b, fb, k0, nb0, tk.mat);
+            else tma_load_4d_pair(b, op.b, fb, 0, k0, nb0 >> 6, tk.mat);
+          }
           if (++st == STAGES) {
             st = 0;
             ph ^= 1u;
@@ -743,6 +751,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         const uint32_t idesc = idesc_bf16_m256(tk.nt, op.a_mn, op.b_mn);
         const uint32_t a_step = op.a_mn ? 2048u : 32u, b_step = op.b_mn ? 2048u : 32u;
         const uint32_t a_lbo = op.a_mn ? 8192u : 16u, b_lbo = op.b_mn ? 8192u : 16u;
+        const bool b_from_a = b_is_a(tk);   // then a_mn == b_mn: the same steps and strides
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int st = it % STAGES;
@@ -752,7 +761,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + st * A_TILE_BYTES), b0 = smem_u32(sB + st * BH_TILE_BYTES);
+          const uint32_t a0 = smem_u32(sA + st * A_TILE_BYTES);
+          const uint32_t b0 = b_from_a ? a0 : smem_u32(sB + st * BH_TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             umma_bf16_pair(dacc, smem_desc_sw128(a0 + kk * a_step, a_lbo, 1024),
