@@ -53,6 +53,40 @@ def test_bank_shapes_and_shape_factor():
     assert O.shape_factor(768, 3072) == 1.0
 
 
+def test_effective_lr_and_decay_of_the_pages_defaults():
+    """With the pages' defaults, the MLP slices (shape factor 2) step at twice the learning rate
+    and every slice decays by lr * wd = 2e-4 per step; an exactly representable case checks
+    that the decay amount is a product, not a sum or a quotient."""
+    g, shapes = _gold("muon_defaults.json"), _gold("bank_shapes.json")
+    lr, wd = g["lr"], g["weight_decay"]
+    assert O.effective_lr(lr, *shapes["mlp"]["view"][1:]) == pytest.approx(0.04, rel=1e-15)
+    assert O.effective_lr(lr, *shapes["attn"]["view"][1:]) == lr
+    assert O.effective_wd(lr, wd) == pytest.approx(2e-4, rel=1e-15)
+    assert O.effective_wd(0.5, 0.25) == 0.125
+    assert O.effective_lr(0.5, 4096, 1024) == 1.0      # sqrt(4) = 2, exact
+
+
+def test_frobenius_scale_of_a_known_norm():
+    """diag(3, 4) has Frobenius norm 5 (and spectral norm 4); the scale is 1 / (5 + eps), and a
+    Gaussian matrix scaled by it has unit Frobenius norm to within eps relative."""
+    assert O.frobenius_scale(np.diag([3.0, 4.0])) == pytest.approx(1.0 / (5.0 + 1e-7), rel=1e-15)
+    assert O.frobenius_scale(np.zeros((3, 5))) == pytest.approx(1e7, rel=1e-15)
+    u = np.random.default_rng(8).standard_normal((40, 70))
+    n = np.linalg.norm(u * O.frobenius_scale(u))
+    assert 1.0 - 1e-7 / np.linalg.norm(u) - 1e-15 <= n < 1.0
+
+
+def test_step_coeffs_forms():
+    """One triple repeats for every step; a schedule gives each step its own triple, in order;
+    a schedule of the wrong length is refused."""
+    one = (3.4445, -4.7750, 2.0315)
+    assert O.step_coeffs(3, one) == [one] * 3
+    sched = [(1.0, 2.0, 3.0), (4.0, 5.0, 6.0)]
+    assert O.step_coeffs(2, sched) == sched
+    with pytest.raises(ValueError):
+        O.step_coeffs(3, sched)
+
+
 def test_bank_view_slot_rule():
     # the stored attention bank (L, 4*d, d) viewed with no copy as (4L, d, d):
     # slot k must be layer k//4, projection k%4
