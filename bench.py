@@ -353,6 +353,8 @@ def run_native(args):
     ns_tflops = fl["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
     mom_gbs = 12.0 * E / (per["momentum"] * 1e-3) / 1e9 if per.get("momentum") else None
     upd_gbs = 10.0 * E / (per["update"] * 1e-3) / 1e9 if per.get("update") else None
+    # NorMuon row statistics: each element of v read once (2 B); the per-row state is negligible
+    row_gbs = 2.0 * E / (per["rowstats"] * 1e-3) / 1e9 if per.get("rowstats") else None
     per_launch_flops = fl["gemm"] * args.steps / max(gemm_launches, 1)
     per_launch_ms = gemm_ms * args.steps / max(gemm_launches, 1)
 
@@ -460,9 +462,12 @@ def run_native(args):
             "ns_tflops": ns_tflops,
             "ns_tflops_dense_equiv": fl["dense_gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None,
             "momentum_gbs": mom_gbs, "update_gbs": upd_gbs,
+            **({"normuon_rowstats_gbs": row_gbs} if row_gbs else {}),
             "fractions": {"ns_of_bf16_sustained": (ns_tflops / tensor_peak) if ns_tflops else None,
                           "momentum_of_hbm": (mom_gbs / hbm_peak) if mom_gbs else None,
-                          "update_of_hbm": (upd_gbs / hbm_peak) if upd_gbs else None, "peaks": pk_kind},
+                          "update_of_hbm": (upd_gbs / hbm_peak) if upd_gbs else None,
+                          **({"normuon_rowstats_of_hbm": row_gbs / hbm_peak} if row_gbs else {}),
+                          "peaks": pk_kind},
             "stages_ms_per_step": per,
             "cpu_baseline": cpu_base,
             "e2e": e2e,

@@ -71,16 +71,32 @@ __global__ void __launch_bounds__(EW_THREADS) k1_kernel(const __grid_constant__ 
   };
 
   if ((B.cols & 7) == 0) {
-    for (int e = e0 + threadIdx.x * 8; e < e1; e += EW_THREADS * 8) {
+    // every load of the thread's part of the chunk first (they may not move past the u
+    // stores, which could alias the gradient), then the arithmetic and stores in element order
+    constexpr int SLICES = EW_CHUNK / (EW_THREADS * 8);
+    uint4 gl[SLICES];
+    float4 ml[SLICES][2];
+#pragma unroll
+    for (int j = 0; j < SLICES; ++j) {
+      const int e = e0 + (j * EW_THREADS + static_cast<int>(threadIdx.x)) * 8;
+      if (e < e1) {
+        gl[j] = *reinterpret_cast<const uint4*>(src + e);
+        if (MOMENTUM) {
+          ml[j][0] = *reinterpret_cast<const float4*>(mom + e);
+          ml[j][1] = *reinterpret_cast<const float4*>(mom + e + 4);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < SLICES; ++j) {
+      const int e = e0 + (j * EW_THREADS + static_cast<int>(threadIdx.x)) * 8;
+      if (e >= e1) break;
       const int row = e / B.cols, col = e - row * B.cols;
-      const uint4 gv = *reinterpret_cast<const uint4*>(src + e);
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      const uint32_t gw[4] = {gl[j].x, gl[j].y, gl[j].z, gl[j].w};
       float bm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (MOMENTUM) {
-        const float4 m0 = *reinterpret_cast<const float4*>(mom + e);
-        const float4 m1 = *reinterpret_cast<const float4*>(mom + e + 4);
-        bm[0] = m0.x; bm[1] = m0.y; bm[2] = m0.z; bm[3] = m0.w;
-        bm[4] = m1.x; bm[5] = m1.y; bm[6] = m1.z; bm[7] = m1.w;
+        bm[0] = ml[j][0].x; bm[1] = ml[j][0].y; bm[2] = ml[j][0].z; bm[3] = ml[j][0].w;
+        bm[4] = ml[j][1].x; bm[5] = ml[j][1].y; bm[6] = ml[j][1].z; bm[7] = ml[j][1].w;
       }
       uint32_t uw[4];
 #pragma unroll
