@@ -34,7 +34,7 @@ def _case(seed, shape, kind="gauss", std=1e-3, dead=()):
 
 # ---------------------------------------------------------------- S1
 
-@pytest.mark.parametrize("shape", [(4, 128, 128), (3, 200, 328), (2, 6, 12), (2, 13, 77), (1, 768, 3072)])
+@pytest.mark.parametrize("shape", [(4, 128, 128), (3, 200, 328), (2, 6, 12), (2, 13, 77), (1, 768, 3072), (5, 1, 1)])
 def test_momentum(nss, shape):
     w, mant, mom, _, g = _case(11, shape, std=1.0)
     gt, mt = to_dev(g), to_dev(mom)
@@ -69,7 +69,7 @@ def test_momentum_edge_coefficients(nss, mu):
 
 # ---------------------------------------------------------------- S5
 
-@pytest.mark.parametrize("shape", [(4, 128, 128), (3, 200, 328), (2, 6, 12), (2, 3072, 768), (1, 7, 9)])
+@pytest.mark.parametrize("shape", [(4, 128, 128), (3, 200, 328), (2, 6, 12), (2, 3072, 768), (1, 7, 9), (5, 1, 1)])
 def test_update(nss, shape):
     w, mant, _, _, _ = _case(12, shape)
     v = synth.v_bits(13, *shape, scale=shape[1] ** -0.5)
@@ -108,6 +108,7 @@ NS_SHAPES = [
     ((2, 300, 520), "gauss"), ((2, 520, 300), "lowrank"),
     ((2, 768, 768), "lowrank"), ((1, 768, 3072), "gauss"), ((2, 3072, 768), "lowrank"),
     ((3, 12, 768), "lowrank"), ((3, 6, 12), "lowrank"), ((2, 64, 64), "gauss"), ((2, 1, 40), "gauss"),
+    ((5, 1, 1), "gauss"), ((2, 40, 1), "gauss"),
     # small min(rows, cols) whose fp32 iteration does not fit in shared memory: workspace path
     ((2, 40, 2000), "gauss"), ((2, 1500, 50), "lowrank"),
     # the largest here: 16 row blocks of A, hundreds of tiles per phase of one matrix
@@ -204,7 +205,7 @@ def _run_step(nss, shape, seed, steps=1, ns_steps=5, kind="gauss", std=1e-3, dea
     return (w, mant, mom, row, g), t, ws
 
 
-@pytest.mark.parametrize("shape", [(4, 128, 128), (3, 328, 200), (2, 200, 328), (10, 6, 12), (1, 12, 768)])
+@pytest.mark.parametrize("shape", [(4, 128, 128), (3, 328, 200), (2, 200, 328), (10, 6, 12), (1, 12, 768), (5, 1, 1)])
 def test_full_step(nss, shape):
     (w, mant, mom, _, g), t, ws = _run_step(nss, shape, 21, std=1.0)
     B, R, C = shape
