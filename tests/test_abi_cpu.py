@@ -101,6 +101,22 @@ def test_banks_of_one_call_share_the_launch_limits(lib):
     assert lib.mb_multi_workspace_bytes(arr, 2, 0, ctypes.byref(out)) == 0
 
 
+def test_a_failing_cuda_call_is_reported(lib):
+    """Where no CUDA device is usable, every call that needs one fails in the CUDA runtime: the
+    library returns MB_ERR_CUDA and keeps the runtime's message, instead of crashing.  The calls
+    used take no device pointers, so nothing can be touched on a machine that has a device."""
+    import torch
+    from newton_schulz_stacked_gb300 import _binding as b
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is usable here")
+    assert lib.mb_sync_status(None) == b.MB_ERR_CUDA
+    assert lib.mb_last_cuda_error()
+    assert lib.mb_selftest_timeout(1000, None) == b.MB_ERR_CUDA
+    assert lib.mb_timing_begin(4) == b.MB_ERR_CUDA
+    assert lib.mb_timing_end(0, None, None, None) == b.MB_ERR_ARG    # the failed begin left no session
+    assert lib.mb_launch_count() == 0
+
+
 def test_workspace_views(lib):
     from newton_schulz_stacked_gb300 import _binding as b
     u, v, p = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
