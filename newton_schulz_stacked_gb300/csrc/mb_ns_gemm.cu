@@ -384,9 +384,14 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
   const int ncols = J.nt >> 1;
   const int cbeg = half * ncols;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-  const bool odd = lane & 1;
-  const uint32_t word_off = 4u * ((lane >> 1) & 3);
   const float ca = P.ca[J.it], cb = P.cb[J.it], cc = P.cc[J.it];
+  // The chunk moves as 8x8 matrices in MMA-fragment order (TMEM loads of 16 lanes,
+  // ldmatrix / stmatrix through the 64-byte swizzle).  For row half g (rows 16g..16g+15)
+  // and column pair p, matrix i covers rows 16g + 8(i & 1) .. and columns 8(2p + (i >> 1)) ..;
+  // this thread addresses row `mrow` (of the half) and column group 2p + `mcol`.
+  const int mrow = 8 * ((lane >> 3) & 1) + (lane & 7);
+  const int mcol = lane >> 4;
+  const uint32_t sD = smem_u32(bufD), sT = smem_u32(bufT);
 
 
   for (int c = 0; c < ncols; c += 32) {
@@ -408,29 +413,28 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
     }
     const bool lo_out = EPI == EPI_APPLY && LO == LO_WRITE && direct;
 
-    // this chunk's input row (and, in the second step's APPLY, X_1's residual), both halves,
-    // taken into registers at the chunk's start so that its slots refill under the chunk's work
+    // this chunk's input (and, in the second step's APPLY, X_1's residual), both row halves,
+    // taken into registers at the chunk's start so that its slots refill under the chunk's
+    // work; register 8g + 4p + i holds matrix i of column pair p of row half g
     uint32_t ex[16], lx[16];
     if (has_ein) {
       in_top_up(F, P, lane);
       const uint32_t slot = F.used % IN_SLOTS;
       if (!mbar_wait_or_abort(&F.full[slot], (F.used / IN_SLOTS) & 1, abort_flag)) return false;
-      const uint8_t* in = F.buf + slot * IN_BOX_BYTES;
+      const uint32_t in = smem_u32(F.buf + slot * IN_BOX_BYTES);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = *reinterpret_cast<const uint4*>(in + sw64(lane, q));
-        ex[4 * q] = v.x; ex[4 * q + 1] = v.y; ex[4 * q + 2] = v.z; ex[4 * q + 3] = v.w;
-      }
+      for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int p = 0; p < 2; ++p) ldmatrix_x4(in + sw64(16 * g + mrow, 2 * p + mcol), ex + 8 * g + 4 * p);
       uint32_t dep = 0;
       if (with_lo) {
         const uint32_t slot2 = (F.used + 1) % IN_SLOTS;
         if (!mbar_wait_or_abort(&F.full[slot2], ((F.used + 1) / IN_SLOTS) & 1, abort_flag)) return false;
-        const uint8_t* inl = F.buf + slot2 * IN_BOX_BYTES;
+        const uint32_t inl = smem_u32(F.buf + slot2 * IN_BOX_BYTES);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = *reinterpret_cast<const uint4*>(inl + sw64(lane, q));
-          lx[4 * q] = v.x; lx[4 * q + 1] = v.y; lx[4 * q + 2] = v.z; lx[4 * q + 3] = v.w;
-        }
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+          for (int p = 0; p < 2; ++p) ldmatrix_x4(inl + sw64(16 * g + mrow, 2 * p + mcol), lx + 8 * g + 4 * p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) dep ^= lx[i];
       }
@@ -447,59 +451,49 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
     if (lane == 0) bulk_wait_read_all();        // the previous chunk's stores have read the buffers
     __syncwarp();
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t* e_cur = ex + 8 * h;
-      const uint32_t* l_cur = lx + 8 * h;
+    for (int g = 0; g < 2; ++g) {
+      // rows 16g..16g+15 of the chunk: column group j's pairs sit in registers 4j (upper
+      // 8 rows) and 4j + 2 (lower 8 rows), as matrix i = 2(j & 1) + (upper ? 0 : 1) of pair j / 2
       uint32_t acc[16];
-      tmem_ld_32x16(tacc + lane_base + static_cast<uint32_t>(cbeg + c + 16 * h), acc);
+      tmem_ld_16x256b_x4(tacc + lane_base + (static_cast<uint32_t>(16 * g) << 16) + static_cast<uint32_t>(cbeg + c),
+                         acc);
       tmem_ld_wait();
-      float o[16];
-      if (EPI == EPI_GRAM) {
+      uint32_t pk[8], pl[8];   // [4p + i], matrix i of column pair p, as the input registers
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = J.alpha * __uint_as_float(acc[i]);
-      } else if (EPI == EPI_POLY) {
+      for (int j = 0; j < 4; ++j) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[2 * i] = fmaf(cc, __uint_as_float(acc[2 * i]), cb * bf16_lo(e_cur[i]));
-          o[2 * i + 1] = fmaf(cc, __uint_as_float(acc[2 * i + 1]), cb * bf16_hi(e_cur[i]));
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float x0 = bf16_lo(e_cur[i]), x1 = bf16_hi(e_cur[i]);
-          if (with_lo) {
-            x0 += bf16_lo(l_cur[i]);
-            x1 += bf16_hi(l_cur[i]);
+        for (int lo8 = 0; lo8 < 2; ++lo8) {
+          const int k = 4 * (j >> 1) + 2 * (j & 1) + lo8;
+          const float a0 = __uint_as_float(acc[4 * j + 2 * lo8]), a1 = __uint_as_float(acc[4 * j + 2 * lo8 + 1]);
+          float o0, o1;
+          if (EPI == EPI_GRAM) {
+            o0 = J.alpha * a0;
+            o1 = J.alpha * a1;
+          } else if (EPI == EPI_POLY) {
+            o0 = fmaf(cc, a0, cb * bf16_lo(ex[8 * g + k]));
+            o1 = fmaf(cc, a1, cb * bf16_hi(ex[8 * g + k]));
+          } else {
+            float x0 = bf16_lo(ex[8 * g + k]), x1 = bf16_hi(ex[8 * g + k]);
+            if (with_lo) {
+              x0 += bf16_lo(lx[8 * g + k]);
+              x1 += bf16_hi(lx[8 * g + k]);
+            }
+            o0 = J.alpha * fmaf(ca, x0, a0);
+            o1 = J.alpha * fmaf(ca, x1, a1);
           }
-          o[2 * i] = J.alpha * fmaf(ca, x0, __uint_as_float(acc[2 * i]));
-          o[2 * i + 1] = J.alpha * fmaf(ca, x1, __uint_as_float(acc[2 * i + 1]));
+          pk[k] = pack_bf16x2(o0, o1);
+          // residual o - bf16(o), row-major in the (otherwise idle) transposed buffer
+          if (lo_out) pl[k] = pack_bf16x2(o0 - bf16_lo(pk[k]), o1 - bf16_hi(pk[k]));
         }
       }
-      uint32_t pk[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
-      if (direct || diag) {
-        *reinterpret_cast<uint4*>(bufD + sw64(lane, 2 * h)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(bufD + sw64(lane, 2 * h + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      }
-      if (mirror || diag) {
-        // transposed words: lanes 2r and 2r+1 swap halves so that each lane writes whole
-        // 32-bit words (rows 2r, 2r+1 of one transposed column): even lane column 2i, odd 2i+1
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t x = __shfl_xor_sync(0xffffffffu, pk[i], 1);
-          const uint32_t w = odd ? ((x >> 16) | (pk[i] & 0xFFFF0000u)) : ((pk[i] & 0xFFFFu) | (x << 16));
-          *reinterpret_cast<uint32_t*>(bufT + sw64(16 * h + 2 * i + (odd ? 1 : 0), lane >> 3) + word_off) = w;
-        }
-      }
-      if (lo_out) {
-        // residual o - bf16(o), row-major in the (otherwise idle) transposed buffer
-        uint32_t pl[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          pl[i] = pack_bf16x2(o[2 * i] - bf16_lo(pk[i]), o[2 * i + 1] - bf16_hi(pk[i]));
-        *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-        *reinterpret_cast<uint4*>(bufT + sw64(lane, 2 * h + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+      for (int p = 0; p < 2; ++p) {
+        if (direct || diag) stmatrix_x4(sD + sw64(16 * g + mrow, 2 * p + mcol), pk + 4 * p);
+        // the transposed matrix (rows 16g + 8(i & 1) .., columns 8j ..) lands at rows 8j ..,
+        // columns 16g + 8(i & 1) .. of the transposed chunk
+        if (mirror || diag)
+          stmatrix_x4_trans(sT + sw64(8 * (2 * p + mcol) + (lane & 7), 2 * g + ((lane >> 3) & 1)), pk + 4 * p);
+        if (lo_out) stmatrix_x4(sT + sw64(16 * g + mrow, 2 * p + mcol), pl + 4 * p);
       }
     }
     if (diag) {
