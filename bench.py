@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -83,11 +84,20 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_text(src: str) -> str:
+    """C++ source without its comments and with runs of whitespace collapsed: what the compiler
+    sees (these sources hold no comment markers inside string literals)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_hash():
+    """Hash of the NS kernel's code (comments and layout excluded), to match profiled counters."""
     h = hashlib.sha256()
     for rel in NS_GEMM_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_text(f.read()).encode())
     return h.hexdigest()[:16]
 
 

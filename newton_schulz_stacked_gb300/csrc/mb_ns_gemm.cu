@@ -59,7 +59,9 @@
 //                   X for APPLY, plus X_1's residual in the second step) arrives
 //                   by TMA in 32x32 boxes through a two-slot ring refilled as each
 //                   chunk is taken, and its results leave through shared memory by
-//                   TMA bulk stores
+//                   TMA bulk stores; a chunk moves as 8x8 matrices in MMA-fragment
+//                   order (16-lane TMEM loads, ldmatrix, stmatrix and, for the
+//                   mirror of a symmetric chunk, stmatrix.trans)
 #include <atomic>
 
 #include "mb_device.cuh"
@@ -242,7 +244,8 @@ __device__ __forceinline__ bool dependency(const Task& k, int& dit, int& dph) {
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a [32][32] bf16 staging
 // buffer laid out as the TMA 64-byte swizzle expects (address bits [4,6) XOR
-// bits [7,9)): row-wise 16-byte writes of a warp then hit distinct banks.
+// bits [7,9)): the eight 16-byte rows of an 8x8 matrix (ldmatrix / stmatrix) then hit
+// distinct banks, and so do row-wise 16-byte accesses of a warp.
 __device__ __forceinline__ uint32_t sw64(int row, int chunk) {
   return static_cast<uint32_t>(row * 64 + 16 * (chunk ^ ((row >> 1) & 3)));
 }
@@ -361,9 +364,9 @@ __device__ __forceinline__ void in_top_up(InFeed& F, const NsParams& P, int lane
   }
 }
 
-// Epilogue of one warp: TMEM lanes of quadrant `quad` (tile rows quad*32 + lane),
-// columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`, taken
-// 16 columns at a time.
+// Epilogue of one warp: TMEM lanes of quadrant `quad` (tile rows quad*32 .. quad*32 + 31),
+// columns [half * nt/2, (half + 1) * nt/2) of the accumulator at `tacc`, taken as
+// 32x32 chunks of two 16-row halves.
 // Each 32x32 chunk is staged in the warp's shared buffer and written with a
 // TMA bulk store; a symmetric phase also stores the transposed chunk at the
 // mirrored position.  A 128-block below the diagonal is not stored at all; in
