@@ -397,3 +397,78 @@ def test_bank_matrices_are_independent():
     for j, k in enumerate(perm):
         np.testing.assert_array_equal(pm["w_bits"][j], full["w_bits"][k])
         np.testing.assert_array_equal(pm["mantissa"][j], full["mantissa"][k])
+
+
+def test_bank_step_diagonal_closed_form():
+    """One whole step on 8 x 2 (tall) slices with a diagonal gradient and a diagonal momentum
+    buffer, each holding one of the two diagonal entries: the step's result follows from the
+    scalars alone.
+
+    mu = 1/2 gives buf = (1/2, 1/2) and u = (3/4, 1/4) on the diagonal, exactly; the quintic
+    of the pages maps each normalised singular value u_i / (||u||_F + 1e-7) through its five
+    steps; the update subtracts lr * sqrt(8 / 2) * v from the decayed weight.  Feeding g or the
+    buffer to Newton-Schulz instead of u, dropping the shape factor, the decay or the sign of
+    the step each changes the result far beyond fp32 rounding."""
+    coef = _gold("ns_coefficients.json")
+    a, b, c, steps = coef["a"], coef["b"], coef["c"], coef["steps"]
+    lr, wd, mu = 0.02, 0.01, 0.5
+    shape = (2, 8, 2)
+    g = np.zeros(shape, np.uint16)
+    buf = np.zeros(shape, np.float32)
+    g[:, 0, 0] = synth.to_bf16_bits(np.array(1.0))
+    buf[:, 1, 1] = 1.0
+    w = np.zeros(shape, np.uint16)
+    m = np.zeros(shape, np.uint16)
+    w[1] = synth.to_bf16_bits(np.ones((8, 2)))           # slice 1 starts at w = 1 everywhere, slice 0 at 0
+    out = O.bank_step(w, m, buf, g, lr, wd, mu)
+
+    u_diag = (0.75, 0.25)
+    norm = math.sqrt(0.75 ** 2 + 0.25 ** 2) + 1e-7
+    v_diag = []
+    for ui in u_diag:
+        x = ui / norm
+        for _ in range(steps):
+            x = a * x + b * x ** 3 + c * x ** 5
+        v_diag.append(x)
+    eff_lr = lr * 2.0                                   # sqrt(max(1, 8 / 2))
+    for k in range(2):
+        buf_expect = np.zeros((8, 2), np.float32)
+        buf_expect[0, 0] = buf_expect[1, 1] = 0.5
+        np.testing.assert_array_equal(out["buf"][k], buf_expect)
+        u_vals = O.bf16_bits_to_f64(out["u"][k])
+        np.testing.assert_array_equal(u_vals[[0, 1], [0, 1]], u_diag)
+        assert np.count_nonzero(u_vals) == 2
+        v_expect = np.zeros((8, 2))
+        v_expect[0, 0], v_expect[1, 1] = v_diag
+        np.testing.assert_allclose(out["v"][k], v_expect, rtol=1e-12, atol=1e-15)
+        w0 = 1.0 if k == 1 else 0.0
+        w_expect = (w0 * (1.0 - lr * wd) - eff_lr * v_expect).astype(np.float32)
+        np.testing.assert_allclose(out["w32"][k], w_expect, rtol=2.0 ** -23, atol=0)
+        hi, lo = O.split_f32(w_expect)
+        np.testing.assert_array_equal(out["w_bits"][k], hi)
+        np.testing.assert_array_equal(out["mantissa"][k], lo)
+
+
+# ---------------------------------------------------------------- the parity comparator
+
+def test_rel_frobenius_known_values():
+    """||x - ref||_F / ||ref||_F on cases whose value is exact in binary floating point, chosen
+    so that a dropped square root, a division by ||ref||^2 or by ||x||, a norm over one axis
+    only, or a comparator that returns 0 gives another value."""
+    eye = np.eye(4)
+    assert O.rel_frobenius(eye, 2.0 * eye) == 0.5             # ||I|| / ||2I|| = 2 / 4
+    assert O.rel_frobenius(2.0 * eye, eye) == 1.0             # ||I|| / ||I||
+    assert O.rel_frobenius([3.0, 0.0], [0.0, 4.0]) == 1.25    # ||(3, -4)|| / 4 = 5 / 4
+    ref = np.ones((4, 4))
+    assert O.rel_frobenius(-ref, ref) == 2.0                  # a sign flip is reported as large
+    x = ref.copy()
+    x[3, 3] += 3.0
+    assert O.rel_frobenius(x, ref) == 0.75                    # one element of 16: 3 / 4
+    x = ref.copy()
+    x[0, :] += 1.0
+    assert O.rel_frobenius(x, ref) == 0.5                     # a whole row: 2 / 4
+    assert O.rel_frobenius(ref, ref) == 0.0
+    assert O.rel_frobenius(np.zeros((2, 3)), np.zeros((2, 3))) == 0.0
+    assert O.rel_frobenius(np.eye(2), np.zeros((2, 2))) == math.inf
+    # it compares values, not bit patterns: -0 equals +0
+    assert O.rel_frobenius(np.array([-0.0, 1.0]), np.array([0.0, 1.0])) == 0.0
