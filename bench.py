@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -46,6 +47,7 @@ def parse():
     p.add_argument("--workload", type=int, default=4, choices=[4, 5, 6])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true", help="skip the GPT-2-medium line added to workload 4's")
     return p.parse_args()
 
 
@@ -191,23 +193,36 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def cpu_oracle_sample(wl, per_bank, seed_step=1):
-    """Time the fp64 oracle on a bounded sample of the workload; extrapolate to one full step."""
+def one_matrix_states(wl, seed):
+    """One matrix's seeded state and gradient per bank (the oracle's cost depends on the shape only)."""
     import numpy as np
-    import oracle as O
     import synth
-    total_est, sampled, desc = 0.0, 0, []
+    out = []
     for bi, spec in enumerate(wl.banks):
-        n = min(per_bank.get(spec.name, 1), spec.batch)
-        rng = np.random.default_rng(seed_step * 100 + bi)
-        idx = sorted(rng.choice(spec.batch, size=n, replace=False).tolist())
+        rng = np.random.default_rng(seed * 100 + bi)
         one = synth.BankSpec(spec.name, 1, spec.rows, spec.cols, spec.grad_kind, spec.grad_std)
         w, mant, mom, row = synth.draw_state(rng, one)
-        g = synth.draw_grad(rng, one)
+        out.append((w, mant, mom, row, synth.draw_grad(rng, one)))
+    return out
+
+
+def oracle_matrix_step(wl, state):
+    """The fp64 oracle's whole step (momentum, Newton-Schulz, NorMuon if on, update) on one matrix."""
+    import oracle as O
+    w, mant, mom, row, g = state
+    O.bank_step(w, mant, mom, g, wl.lr, wl.wd, wl.mu, wl.ns_steps,
+                normuon_beta2=wl.beta2 if wl.normuon else None, row_state=row)
+
+
+def cpu_oracle_sample(wl, per_bank, seed_step=1):
+    """Time the fp64 oracle on a bounded sample of the workload; extrapolate to one full step."""
+    total_est, sampled, desc = 0.0, 0, []
+    states = one_matrix_states(wl, seed_step)
+    for bi, spec in enumerate(wl.banks):
+        n = min(per_bank.get(spec.name, 1), spec.batch)
         t0 = time.perf_counter()
-        for _ in idx:
-            O.bank_step(w, mant, mom, g, wl.lr, wl.wd, wl.mu, wl.ns_steps,
-                        normuon_beta2=wl.beta2 if wl.normuon else None, row_state=row)
+        for _ in range(n):
+            oracle_matrix_step(wl, states[bi])
         dt = time.perf_counter() - t0
         total_est += dt / n * spec.batch
         sampled += n
@@ -234,6 +249,19 @@ def cores():
 
 # ---------------------------------------------------------------- reference arm
 
+# Fraction of a bank-step that one reference step processes: the same share of every bank, so
+# that the work done is that fraction of the whole step whatever each bank costs.
+REF_FRACTION = {4: 1 / 8, 5: 1 / 48, 6: 1 / 8}
+
+
+def ref_window(batch, f, k):
+    """Slots of a bank that reference step k processes: a window of f * batch slots that moves on
+    by that much every step (cumulative floors), so consecutive steps cover the bank in turn and
+    any K steps process floor-differences summing to K * f * batch within one slot."""
+    lo, hi = math.floor(k * batch * f), math.floor((k + 1) * batch * f)
+    return [i % batch for i in range(lo, hi)]
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -245,26 +273,40 @@ def run_reference(args):
             os.environ[var] = str(host_cores())
     import synth
     wl = synth.WORKLOADS[args.workload]
-    sample = {"attn": 1, "mlp": 1, "smear_gate": 1, "attn_gate": 10}
-    for _ in range(args.warmup):
-        cpu_oracle_sample(wl, sample, seed_step=0)
-    ests = []
-    desc = ""
+    f = REF_FRACTION[args.workload]
+    states = one_matrix_states(wl, 1)
+
+    def ref_step(k):
+        done = {}
+        for bi, spec in enumerate(wl.banks):
+            slots = ref_window(spec.batch, f, k)
+            for _ in slots:
+                oracle_matrix_step(wl, states[bi])
+            done[spec.name] = done.get(spec.name, 0) + len(slots)
+        return done
+
+    for k in range(args.warmup):
+        ref_step(k)
+    processed = {}
     t0 = time.perf_counter()
-    for k in range(args.steps):
-        est, _, desc = cpu_oracle_sample(wl, sample, seed_step=k + 1)
-        ests.append(est)
+    for k in range(args.warmup, args.warmup + args.steps):
+        for name, n in ref_step(k).items():
+            processed[name] = processed.get(name, 0) + n
     wall = time.perf_counter() - t0
-    est = statistics.mean(ests)
-    value = 1.0 / est
+    # the banks of the window's width f * batch (an integer for the large banks) make exactly
+    # steps * f bank-steps; the small gate banks rotate one matrix at a time within that share
+    work = args.steps * f
+    value = work / wall
+    desc = ", ".join(f"{processed.get(b.name, 0)} of {b.name} (batch {b.batch})" for b in wl.banks)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64 banks)",
         "config": config_of(wl, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
-                         "sample": f"each step times the fp64 oracle on {desc} and scales to the full step; "
-                                   f"{args.steps} steps took {wall:.1f} s"},
+                         "sample": f"each timed step runs the fp64 oracle's whole step on 1/{round(1 / f)} of "
+                                   f"every bank (a window moving through the slots); {args.steps} steps "
+                                   f"processed {desc} = {work:.3f} bank-steps in {wall:.2f} s"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -284,8 +326,93 @@ def config_of(wl, args):
 
 # ---------------------------------------------------------------- native arm
 
+class DeviceWorkload:
+    """A workload's banks resident on one GPU (two alternating gradient draws), stepped through
+    muon_multi_step, and the device-timed measurement of K steps."""
+
+    def __init__(self, nss, wl, dev):
+        import numpy as np
+        import torch
+        import synth
+        self.nss, self.wl, self.dev = nss, wl, dev
+        self.shapes = shapes_of(wl)
+        t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+        self.banks, self.grads, self.grads_host = [], [], []
+        for bi, spec in enumerate(wl.banks):
+            w, mant, mom, row = synth.init_state(wl.wid, bi)
+            g_steps = [synth.grad(wl.wid, s, bi) for s in (1, 2)]
+            self.grads.append([t16(g) for g in g_steps])
+            self.grads_host.append([torch.from_numpy(g.view(np.int16)).pin_memory() for g in g_steps])
+            self.banks.append(nss.BankState(t16(w), self.grads[-1][0], torch.from_numpy(mom).to(dev), t16(mant),
+                                            torch.from_numpy(row).to(dev) if wl.normuon else None))
+        self.ws = torch.empty(nss.mb_multi_workspace_bytes(self.banks, wl.normuon), dtype=torch.uint8, device=dev)
+
+    def step(self, k):
+        for b, g in zip(self.banks, self.grads):
+            b.grad = g[k & 1]
+        self.run_step()
+
+    def run_step(self):
+        wl = self.wl
+        self.nss.muon_multi_step(self.banks, wl.lr, wl.wd, wl.mu, normuon=wl.normuon, beta2=wl.beta2,
+                                 ns_steps=wl.ns_steps, workspace=self.ws)
+
+    def timed(self, steps, warmup, world, gpu_index):
+        """W warm-up steps, then K steps timed with CUDA events on the launching stream (barrier and
+        synchronise on both sides, max over ranks), the library's stage events and launch counter over
+        the same steps, and the SM clocks sampled meanwhile."""
+        import torch
+        import torch.distributed as dist
+        nss = self.nss
+        for k in range(max(warmup, 3)):
+            self.step(k)
+        torch.cuda.synchronize()
+        if nss.mb_sync_status() != 0:
+            raise RuntimeError("device-side status set during warm-up")
+        stream = torch.cuda.current_stream()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = nss.mb_launch_count()
+        with ClockSampler(gpu_index) as clocks:
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            with nss.StageTimer(max_marks=64 * steps + 64) as timer:
+                ev0.record(stream)
+                for k in range(steps):
+                    self.step(k)
+                ev1.record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+        launches = nss.mb_launch_count() - n0
+        elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), self.dev)
+        if nss.mb_sync_status() != 0:
+            raise RuntimeError("device-side status set during the timed steps")
+        return dict(elapsed_ms=elapsed_ms, stages=timer.totals(), launches=launches, clocks=clocks.summary(),
+                    steps=steps)
+
+    def rates(self, t):
+        """Per-stage throughput from one timed() result: NS TFLOP/s (algorithmic flops of the fused
+        launch over its stage time) and the element-wise stages' GB/s over their algorithmic bytes."""
+        steps = t["steps"]
+        per = {k: v[0] / steps for k, v in t["stages"].items()}
+        gemm_ms = per.get("ns_gemm", 0.0)
+        gemm_launches = t["stages"].get("ns_gemm", (0, 0))[1]
+        fl = ns_flops(self.shapes, self.wl.ns_steps)
+        E = elems(self.shapes)
+        r = dict(per=per, flops=fl, gemm_ms=gemm_ms, gemm_launches=gemm_launches)
+        r["ns_tflops"] = fl["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
+        r["ns_tflops_dense_equiv"] = fl["dense_gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
+        r["momentum_gbs"] = 12.0 * E / (per["momentum"] * 1e-3) / 1e9 if per.get("momentum") else None
+        r["update_gbs"] = 10.0 * E / (per["update"] * 1e-3) / 1e9 if per.get("update") else None
+        # NorMuon row statistics: each element of v read once (2 B); the per-row state is negligible
+        r["normuon_rowstats_gbs"] = 2.0 * E / (per["rowstats"] * 1e-3) / 1e9 if per.get("rowstats") else None
+        r["flops_per_launch"] = fl["gemm"] * steps / max(gemm_launches, 1)
+        r["ms_per_launch"] = gemm_ms * steps / max(gemm_launches, 1)
+        return r
+
+
 def run_native(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -301,83 +428,60 @@ def run_native(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     nss.load_library()
+    gpu_index = torch.cuda.current_device() if world == 1 else local
 
     wl = synth.WORKLOADS[args.workload]
-    shapes = shapes_of(wl)
-    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
-    banks, grads, grads_host = [], [], []
-    for bi, spec in enumerate(wl.banks):
-        w, mant, mom, row = synth.init_state(wl.wid, bi)
-        g_steps = [synth.grad(wl.wid, s, bi) for s in (1, 2)]
-        grads.append([t16(g) for g in g_steps])
-        grads_host.append([torch.from_numpy(g.view(np.int16)).pin_memory() for g in g_steps])
-        banks.append(nss.BankState(t16(w), grads[-1][0], torch.from_numpy(mom).to(dev), t16(mant),
-                                   torch.from_numpy(row).to(dev) if wl.normuon else None))
-    ws = torch.empty(nss.mb_multi_workspace_bytes(banks, wl.normuon), dtype=torch.uint8, device=dev)
-
-    def step(k):
-        for b, g in zip(banks, grads):
-            b.grad = g[k & 1]
-        nss.muon_multi_step(banks, wl.lr, wl.wd, wl.mu, normuon=wl.normuon, beta2=wl.beta2, ns_steps=wl.ns_steps,
-                            workspace=ws)
-
-    for k in range(max(args.warmup, 3)):
-        step(k)
-    torch.cuda.synchronize()
-    if nss.mb_sync_status() != 0:
-        raise RuntimeError("device-side status set during warm-up")
-
-    stream = torch.cuda.current_stream()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n0 = nss.mb_launch_count()
-    with ClockSampler(torch.cuda.current_device() if world == 1 else local) as clocks:
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        with nss.StageTimer(max_marks=64 * args.steps + 64) as timer:
-            ev0.record(stream)
-            for k in range(args.steps):
-                step(k)
-            ev1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-    launches = nss.mb_launch_count() - n0
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
-    if nss.mb_sync_status() != 0:
-        raise RuntimeError("device-side status set during the timed steps")
-
+    run = DeviceWorkload(nss, wl, dev)
+    banks, grads_host, ws = run.banks, run.grads_host, run.ws
+    t = run.timed(args.steps, args.warmup, world, gpu_index)
+    elapsed_ms, launches = t["elapsed_ms"], t["launches"]
     ms_per_step = elapsed_ms / args.steps
     value = job_rate(world, args.steps, elapsed_ms)
+    r = run.rates(t)
+    per, ns_tflops = r["per"], r["ns_tflops"]
+    mom_gbs, upd_gbs, row_gbs = r["momentum_gbs"], r["update_gbs"], r["normuon_rowstats_gbs"]
 
-    # per-stage device time from the library's stage events (same stream, same timed steps)
-    tot = timer.totals()
-    per = {k: v[0] / args.steps for k, v in tot.items()}
-    gemm_ms = per.get("ns_gemm", 0.0)
-    gemm_launches = tot.get("ns_gemm", (0, 0))[1]
-    fl = ns_flops(shapes, wl.ns_steps)
-    E = elems(shapes)
     pk, pk_kind = peaks()
-    tensor_peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # the timed region is tens to hundreds of milliseconds of steps: the burst peak applies; the
+    # fraction of the sustained (power-capped, seconds-long) peak is reported beside it
+    burst_peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained_peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     hbm_peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    ns_tflops = fl["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
-    mom_gbs = 12.0 * E / (per["momentum"] * 1e-3) / 1e9 if per.get("momentum") else None
-    upd_gbs = 10.0 * E / (per["update"] * 1e-3) / 1e9 if per.get("update") else None
-    # NorMuon row statistics: each element of v read once (2 B); the per-row state is negligible
-    row_gbs = 2.0 * E / (per["rowstats"] * 1e-3) / 1e9 if per.get("rowstats") else None
-    per_launch_flops = fl["gemm"] * args.steps / max(gemm_launches, 1)
-    per_launch_ms = gemm_ms * args.steps / max(gemm_launches, 1)
-
     roofline = {
         "bound": "tensor",
         "kernel": "ns_fused_kernel: all Newton-Schulz steps (A=XX^T, B=bA+cAA, X=aX+BX), %d launch(es) per step" % (
-            gemm_launches // args.steps),
-        "achieved": ns_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
-        "frac": (ns_tflops / tensor_peak) if ns_tflops else None,
-        "peak_kind": f"{pk_kind} bf16 sustained (kernel timed inside a long step loop)",
-        "flops_per_launch": per_launch_flops, "ms_per_launch": per_launch_ms,
+            r["gemm_launches"] // args.steps),
+        "achieved": ns_tflops, "peak": burst_peak, "unit": "TFLOP/s",
+        "frac": (ns_tflops / burst_peak) if ns_tflops else None,
+        "peak_kind": f"{pk_kind} bf16 burst (the timed region lasts {elapsed_ms:.0f} ms)",
+        "frac_of_sustained": (ns_tflops / sustained_peak) if ns_tflops else None,
+        "flops_per_launch": r["flops_per_launch"], "ms_per_launch": r["ms_per_launch"],
         "traffic": profiled_traffic(args.workload),
     }
+
+    extra = None
+    if world == 1 and args.workload == 4 and not args.no_extra:
+        # the largest configuration (GPT-2-medium banks with NorMuon), device-timed after the
+        # headline; reported beside it, not in place of it
+        wl5 = synth.WORKLOADS[5]
+        run5 = DeviceWorkload(nss, wl5, dev)
+        k5 = max(3, min(args.steps, 20))
+        t5 = run5.timed(k5, 3, world, gpu_index)
+        r5 = run5.rates(t5)
+        extra = {
+            "workload": config_of(wl5, args)["workload"], "steps": k5, "warmup": 3,
+            "value": job_rate(world, k5, t5["elapsed_ms"]), "unit": UNIT,
+            "ms_per_step": t5["elapsed_ms"] / k5,
+            "ns_tflops": r5["ns_tflops"],
+            "ns_frac_of_burst": (r5["ns_tflops"] / burst_peak) if r5["ns_tflops"] else None,
+            "ns_frac_of_sustained": (r5["ns_tflops"] / sustained_peak) if r5["ns_tflops"] else None,
+            "momentum_gbs": r5["momentum_gbs"], "update_gbs": r5["update_gbs"],
+            "normuon_rowstats_gbs": r5["normuon_rowstats_gbs"],
+            "normuon_rowstats_of_hbm": (r5["normuon_rowstats_gbs"] / hbm_peak) if r5["normuon_rowstats_gbs"] else None,
+            "stages_ms_per_step": r5["per"], "gpu_launches": t5["launches"], "clocks": t5["clocks"],
+        }
+        del run5
+        torch.cuda.empty_cache()
 
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -470,10 +574,11 @@ def run_native(args):
             "config": config_of(wl, args),
             "roofline": roofline,
             "ns_tflops": ns_tflops,
-            "ns_tflops_dense_equiv": fl["dense_gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None,
+            "ns_tflops_dense_equiv": r["ns_tflops_dense_equiv"],
             "momentum_gbs": mom_gbs, "update_gbs": upd_gbs,
             **({"normuon_rowstats_gbs": row_gbs} if row_gbs else {}),
-            "fractions": {"ns_of_bf16_sustained": (ns_tflops / tensor_peak) if ns_tflops else None,
+            "fractions": {"ns_of_bf16_burst": (ns_tflops / burst_peak) if ns_tflops else None,
+                          "ns_of_bf16_sustained": (ns_tflops / sustained_peak) if ns_tflops else None,
                           "momentum_of_hbm": (mom_gbs / hbm_peak) if mom_gbs else None,
                           "update_of_hbm": (upd_gbs / hbm_peak) if upd_gbs else None,
                           **({"normuon_rowstats_of_hbm": row_gbs / hbm_peak} if row_gbs else {}),
@@ -482,7 +587,8 @@ def run_native(args):
             "cpu_baseline": cpu_base,
             "e2e": e2e,
             "gpu_launches": launches,
-            "clocks": clocks.summary(),
+            "clocks": t["clocks"],
+            **({"gpt2_medium_normuon": extra} if extra else {}),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

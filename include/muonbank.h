@@ -30,7 +30,7 @@
  *                  formula; this library reads it as): per row i of the
  *                  stored matrix q_i = mean_j v_ij^2, s_i <- beta2 s_i +
  *                  (1-beta2) q_i, v_ij <- v_ij / sqrt(max(s_i, 1e-10)), then
- *                  v is rescaled to its Frobenius norm before S6.
+ *                  v is rescaled to its Frobenius norm before S5.
  *
  * Conventions shared by every entry point
  *   - Buffers are device pointers owned by the caller, row-major and

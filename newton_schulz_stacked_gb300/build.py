@@ -8,8 +8,11 @@ entry-point query, so no libcuda link is needed).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
+import re
 import shutil
+import signal
 import subprocess
 import sys
 
@@ -25,9 +28,41 @@ CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
           "--diag-suppress", "177"]
 # the compiler's NVVM stage (cicc) on the aarch64 hosts sometimes dies with a segmentation
 # fault on the tensor-core source (about one compile in six to one in three, on the same
-# inputs; not its stack: on x86 the file compiles within a 1 MiB stack); a crashed file is
-# compiled again on its own, up to this many attempts in all (all failing: ~5e-5 at 1 in 3)
+# inputs; not its stack: on x86 the file compiles within a 1 MiB stack); a file whose
+# compiler crashed is compiled again on its own, up to this many attempts in all (all
+# failing: ~5e-5 at 1 in 3).  Ordinary compile errors fail the build at once.
 COMPILE_ATTEMPTS = 9
+_DIAGNOSTIC = re.compile(r"\berror\b", re.IGNORECASE)
+
+
+def _crashed(r) -> bool:
+    """Whether a compile failed because a compiler process died on a signal (not on a diagnostic):
+    nvcc itself killed by one, or nvcc reporting a stage that was, with no error message."""
+    if r.returncode == 0:
+        return False
+    if r.returncode < 0 or r.returncode == 128 + signal.SIGSEGV:
+        return True
+    text = (r.stdout or "") + (r.stderr or "")
+    return "Segmentation fault" in text and not _DIAGNOSTIC.search(text)
+
+
+def _flags_stamp(extra_flags) -> str:
+    """Hash of the compiler, architecture and flags a library is built with."""
+    return hashlib.sha256("\0".join([*ARCH, *CFLAGS, *extra_flags]).encode()).hexdigest()
+
+
+def _stamp_path() -> str:
+    return LIB_PATH + ".flags"
+
+
+def _up_to_date(extra_flags) -> bool:
+    if not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < _deps_mtime():
+        return False
+    try:
+        with open(_stamp_path()) as f:
+            return f.read().strip() == _flags_stamp(extra_flags)
+    except OSError:
+        return False
 
 
 def _nvcc() -> str:
@@ -48,8 +83,10 @@ def _deps_mtime():
 
 
 def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library if a source is newer than it; returns its path."""
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _deps_mtime():
+    """Compile and link the library if a source is newer than it or it was built with other flags;
+    returns its path."""
+    extra_flags = list(extra_flags)
+    if not force and _up_to_date(extra_flags):
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
@@ -66,7 +103,7 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
         results = list(ex.map(compile_one, zip(srcs, objs)))
     for i, (cmd, r) in enumerate(results):
         for _ in range(COMPILE_ATTEMPTS - 1):
-            if r.returncode == 0:
+            if not _crashed(r):
                 break
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr + "retrying this file alone\n")
             cmd, r = compile_one((srcs[i], objs[i]))
@@ -81,6 +118,8 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         raise RuntimeError("link of libmuonbank.so failed")
     os.replace(tmp, LIB_PATH)
+    with open(_stamp_path(), "w") as f:
+        f.write(_flags_stamp(extra_flags) + "\n")
     return LIB_PATH
 
 

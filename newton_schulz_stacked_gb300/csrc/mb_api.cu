@@ -950,28 +950,12 @@ int noalloc_scratch(void** out) {
 extern "C" int mb_newton_schulz_noalloc(const void* u_bf16, void* v_bf16, mb_shape shape, int ns_steps,
                                         void* cuda_stream) {
   MB_TRY(check_shape(shape));
-  MB_TRY(check_ptr(u_bf16));
-  MB_TRY(check_ptr(v_bf16));
-  if (ns_steps < 0 || ns_steps > MAX_NS_STEPS) return MB_ERR_NS_STEPS;
   const Layout L = make_layout(shape, 0, 0);
   if (L.end > static_cast<size_t>(MB_NOALLOC_SCRATCH_BYTES)) return MB_ERR_SCRATCH_LIMIT;
   DeviceState* ds = nullptr;
   MB_TRY(device_state(&ds));
   void* scratch = nullptr;
   MB_TRY(noalloc_scratch(&scratch));
-  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  Bank k{};
-  k.grad = static_cast<const uint16_t*>(u_bf16);
-  k.L = L;
-  k.ws = static_cast<uint8_t*>(scratch);
-  mark(MB_MARK_BEGIN, st);
-  MB_TRY(stage_k1(&k, 1, false, 0.f, st, ds));
-  MB_TRY(stage_ns(&k, 1, ns_steps, st, ds));
-  EwParams p = ew_params(&k, 1, [&](const Bank& bk, EwBank& e) {
-    e.xin = bk.at<uint16_t>(bk.L.x[final_buffer(ns_steps)]);
-    e.xout = static_cast<uint16_t*>(v_bf16);
-    e.out_ld = bk.L.cols;
-  });
-  MB_LAUNCH(launch_unpack(p, st), p.total_blocks > 0, MB_MARK_NS0, st);
-  return MB_OK;
+  // the same stage as mb_newton_schulz, with the fixed array as its workspace
+  return ns_stage(u_bf16, v_bf16, shape, ns_steps, nullptr, scratch, MB_NOALLOC_SCRATCH_BYTES, cuda_stream);
 }

@@ -58,3 +58,34 @@ def test_a_file_that_always_crashes_fails_the_build(sandbox, monkeypatch):
     assert calls.count("mb_ns_gemm.cu") == B.COMPILE_ATTEMPTS == 9   # the parallel attempt and eight retries
     assert "link" not in calls
     assert not os.path.exists(B.LIB_PATH)
+
+
+def test_a_compile_error_fails_at_once(sandbox, monkeypatch):
+    """An ordinary diagnostic is not a crash: the file is not compiled again."""
+    calls = []
+
+    def run(cmd, capture_output=True, text=True):
+        src = cmd[cmd.index("-c") + 1] if "-c" in cmd else None
+        calls.append(os.path.basename(src) if src else "link")
+        if src and src.endswith("mb_api.cu"):
+            return types.SimpleNamespace(returncode=2, stdout="", stderr='mb_api.cu(1): error: identifier "x" is undefined\n')
+        open(cmd[cmd.index("-o") + 1], "wb").close()
+        return types.SimpleNamespace(returncode=0, stdout="", stderr="")
+
+    monkeypatch.setattr(B, "subprocess", types.SimpleNamespace(run=run))
+    with pytest.raises(RuntimeError, match="mb_api.cu"):
+        B.build_library(force=True)
+    assert calls.count("mb_api.cu") == 1 and "link" not in calls
+
+
+def test_a_library_built_with_other_flags_is_rebuilt(sandbox, monkeypatch):
+    calls = []
+    monkeypatch.setattr(B, "subprocess", _fake_compiler({}, calls))
+    B.build_library(extra_flags=["-DPROBE=1"])
+    n = calls.count("link")
+    B.build_library(extra_flags=["-DPROBE=1"])          # same flags, sources unchanged: reused
+    assert calls.count("link") == n
+    B.build_library()                                   # other flags: built again
+    assert calls.count("link") == n + 1
+    B.build_library()
+    assert calls.count("link") == n + 1
