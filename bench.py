@@ -34,7 +34,8 @@ sys.path.insert(0, ROOT)
 METRIC = "Muon bank-steps/sec & NS TFLOP/s vs bf16 peak; update GB/s vs HBM peak"
 UNIT = "bank-steps/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-NS_GEMM_SOURCES = ["newton_schulz_stacked_gb300/csrc/mb_ns_gemm.cu", "newton_schulz_stacked_gb300/csrc/mb_device.cuh",
+NS_GEMM_SOURCES = ["newton_schulz_stacked_gb300/csrc/mb_ns_kernel.cuh", "newton_schulz_stacked_gb300/csrc/mb_ns_gemm.cu",
+                   "newton_schulz_stacked_gb300/csrc/mb_device.cuh",
                    "newton_schulz_stacked_gb300/csrc/mb_internal.h"]
 
 
@@ -48,6 +49,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true", help="skip the GPT-2-medium line added to workload 4's")
+    p.add_argument("--step-flags", type=int, default=0,
+                   help="MB_STEP_* options of the step (1: update in the last Newton-Schulz epilogue, "
+                        "2: NorMuon row sums there); 0, the library's default path, is what is reported")
     return p.parse_args()
 
 
@@ -75,6 +79,24 @@ def ns_flops(shapes, ns_steps):
 
 def elems(shapes):
     return sum(B * R * C for (B, R, C) in shapes)
+
+
+STEP_FUSE_UPDATE, STEP_FUSE_ROWSTATS = 1, 2     # the library's MB_STEP_* options
+
+
+def last_epilogue_share(wl, flags):
+    """Elements whose last Newton-Schulz epilogue also finishes the step, as the MB_STEP_* flags
+    ask: without NorMuon it applies the update (tensor-core banks whose columns are a multiple of
+    8, at least 3 steps); with NorMuon it sums v^2 per row, so the row statistics make no pass
+    over v."""
+    n = 0
+    for b in wl.banks:
+        if min(b.rows, b.cols) <= 64 or wl.ns_steps < 3:
+            continue
+        if (wl.normuon and flags & STEP_FUSE_ROWSTATS) or (
+                not wl.normuon and flags & STEP_FUSE_UPDATE and b.cols % 8 == 0):
+            n += b.batch * b.rows * b.cols
+    return n
 
 
 def peaks():
@@ -321,6 +343,7 @@ def config_of(wl, args):
         "l2": "no flush: inputs larger than L2 (%.2f GB of step state read and written per step)" % (
             elems(shapes_of(wl)) * (2 + 2 + 4 + 2) / 1e9),
         "parallelism": f"replicas x{args.gpus}",
+        **({"step_flags": args.step_flags} if getattr(args, "step_flags", 0) else {}),
     }
 
 
@@ -330,11 +353,11 @@ class DeviceWorkload:
     """A workload's banks resident on one GPU (two alternating gradient draws), stepped through
     muon_multi_step, and the device-timed measurement of K steps."""
 
-    def __init__(self, nss, wl, dev):
+    def __init__(self, nss, wl, dev, flags=0):
         import numpy as np
         import torch
         import synth
-        self.nss, self.wl, self.dev = nss, wl, dev
+        self.nss, self.wl, self.dev, self.flags = nss, wl, dev, flags
         self.shapes = shapes_of(wl)
         t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
         self.banks, self.grads, self.grads_host = [], [], []
@@ -355,7 +378,7 @@ class DeviceWorkload:
     def run_step(self):
         wl = self.wl
         self.nss.muon_multi_step(self.banks, wl.lr, wl.wd, wl.mu, normuon=wl.normuon, beta2=wl.beta2,
-                                 ns_steps=wl.ns_steps, workspace=self.ws)
+                                 ns_steps=wl.ns_steps, workspace=self.ws, flags=self.flags)
 
     def timed(self, steps, warmup, world, gpu_index):
         """W warm-up steps, then K steps timed with CUDA events on the launching stream (barrier and
@@ -400,13 +423,24 @@ class DeviceWorkload:
         gemm_launches = t["stages"].get("ns_gemm", (0, 0))[1]
         fl = ns_flops(self.shapes, self.wl.ns_steps)
         E = elems(self.shapes)
+        # elements the update kernel and the row-statistics pass still handle (the rest are done
+        # in the last Newton-Schulz epilogue; their bytes are then part of the fused launch's time)
+        fused = last_epilogue_share(self.wl, self.flags)
+        E_upd = E - fused if not self.wl.normuon else E
+        E_row = E - fused if self.wl.normuon else 0
         r = dict(per=per, flops=fl, gemm_ms=gemm_ms, gemm_launches=gemm_launches)
         r["ns_tflops"] = fl["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
         r["ns_tflops_dense_equiv"] = fl["dense_gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
         r["momentum_gbs"] = 12.0 * E / (per["momentum"] * 1e-3) / 1e9 if per.get("momentum") else None
-        r["update_gbs"] = 10.0 * E / (per["update"] * 1e-3) / 1e9 if per.get("update") else None
+        # a GB/s figure only for a pass over most of the elements (not for a few gate matrices)
+        r["update_gbs"] = (10.0 * E_upd / (per["update"] * 1e-3) / 1e9
+                           if per.get("update") and E_upd >= 0.5 * E else None)
         # NorMuon row statistics: each element of v read once (2 B); the per-row state is negligible
-        r["normuon_rowstats_gbs"] = 2.0 * E / (per["rowstats"] * 1e-3) / 1e9 if per.get("rowstats") else None
+        r["normuon_rowstats_gbs"] = (2.0 * E_row / (per["rowstats"] * 1e-3) / 1e9
+                                     if per.get("rowstats") and E_row >= 0.5 * E else None)
+        r["last_epilogue"] = (None if not fused else
+                              ("row sums of v^2 for %d of %d elements" if self.wl.normuon else
+                               "the update for %d of %d elements") % (fused, E))
         r["flops_per_launch"] = fl["gemm"] * steps / max(gemm_launches, 1)
         r["ms_per_launch"] = gemm_ms * steps / max(gemm_launches, 1)
         return r
@@ -431,7 +465,7 @@ def run_native(args):
     gpu_index = torch.cuda.current_device() if world == 1 else local
 
     wl = synth.WORKLOADS[args.workload]
-    run = DeviceWorkload(nss, wl, dev)
+    run = DeviceWorkload(nss, wl, dev, args.step_flags)
     banks, grads_host, ws = run.banks, run.grads_host, run.ws
     t = run.timed(args.steps, args.warmup, world, gpu_index)
     elapsed_ms, launches = t["elapsed_ms"], t["launches"]
@@ -464,7 +498,7 @@ def run_native(args):
         # the largest configuration (GPT-2-medium banks with NorMuon), device-timed after the
         # headline; reported beside it, not in place of it
         wl5 = synth.WORKLOADS[5]
-        run5 = DeviceWorkload(nss, wl5, dev)
+        run5 = DeviceWorkload(nss, wl5, dev, args.step_flags)
         k5 = max(3, min(args.steps, 20))
         t5 = run5.timed(k5, 3, world, gpu_index)
         r5 = run5.rates(t5)
@@ -478,6 +512,7 @@ def run_native(args):
             "momentum_gbs": r5["momentum_gbs"], "update_gbs": r5["update_gbs"],
             "normuon_rowstats_gbs": r5["normuon_rowstats_gbs"],
             "normuon_rowstats_of_hbm": (r5["normuon_rowstats_gbs"] / hbm_peak) if r5["normuon_rowstats_gbs"] else None,
+            "last_newton_schulz_epilogue_also_does": r5["last_epilogue"],
             "stages_ms_per_step": r5["per"], "gpu_launches": t5["launches"], "clocks": t5["clocks"],
         }
         del run5
@@ -535,7 +570,7 @@ def run_native(args):
                     bank.grad = g
                     bank.bank_copy = sn
                 nss.muon_multi_step(banks, wl.lr, wl.wd, wl.mu, normuon=wl.normuon, beta2=wl.beta2,
-                                    ns_steps=wl.ns_steps, workspace=ws)
+                                    ns_steps=wl.ns_steps, workspace=ws, flags=args.step_flags)
                 ev_gfree[b_].record(main_s)
                 ev_snap[b_].record(main_s)
                 with torch.cuda.stream(d2h_s):
@@ -577,6 +612,7 @@ def run_native(args):
             "ns_tflops_dense_equiv": r["ns_tflops_dense_equiv"],
             "momentum_gbs": mom_gbs, "update_gbs": upd_gbs,
             **({"normuon_rowstats_gbs": row_gbs} if row_gbs else {}),
+            "last_newton_schulz_epilogue_also_does": r["last_epilogue"],
             "fractions": {"ns_of_bf16_burst": (ns_tflops / burst_peak) if ns_tflops else None,
                           "ns_of_bf16_sustained": (ns_tflops / sustained_peak) if ns_tflops else None,
                           "momentum_of_hbm": (mom_gbs / hbm_peak) if mom_gbs else None,

@@ -132,6 +132,27 @@ int muon_multi_step(const mb_bank_desc* banks, int n_banks, float lr, float wd, 
                     int normuon, float beta2, int ns_steps, void* workspace,
                     size_t workspace_bytes, void* cuda_stream);
 
+/* Options of muon_multi_step_ex.  Both move a pass over the step's elements into the
+ * epilogue of the last Newton-Schulz GEMM (the tensor-core kernel then launches a second
+ * instantiation that carries this code); both were measured and are off by default:
+ *   MB_STEP_FUSE_UPDATE    without NorMuon: S5 runs in that epilogue on banks with
+ *                          min(rows, cols) > 64 and cols a multiple of 8 (with at least 3
+ *                          Newton-Schulz steps), reading v as it is stored; the separate
+ *                          update pass then covers only the other banks.  Same bits as the
+ *                          default path.  On the GPT-2-small step it made the step slower
+ *                          (1.35 vs 1.14 ms on one GB300): the epilogue, already the
+ *                          Newton-Schulz kernel's bound, waits on the bank and mantissa loads.
+ *   MB_STEP_FUSE_ROWSTATS  with NorMuon: the row sums of v^2 come from that epilogue (per
+ *                          32-column chunk, added in a fixed order by the row-scale pass)
+ *                          instead of a pass that reads v again.  Same results up to fp32
+ *                          summation order; measured even on the GPT-2-medium step.
+ * Unknown bits: MB_ERR_ARG.  v is still stored in the workspace (mb_workspace_views). */
+#define MB_STEP_FUSE_UPDATE 1u
+#define MB_STEP_FUSE_ROWSTATS 2u
+int muon_multi_step_ex(const mb_bank_desc* banks, int n_banks, float lr, float wd, float mu,
+                       int normuon, float beta2, int ns_steps, unsigned flags, void* workspace,
+                       size_t workspace_bytes, void* cuda_stream);
+
 /* muon_multi_step with each bank's hyperparameters read from device memory when
  * the step runs, so that a captured CUDA graph of the step can be replayed with
  * new values ("Unified zero-copy optimizer" write-up, section 4: all banks' step

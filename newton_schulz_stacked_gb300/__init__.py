@@ -16,7 +16,7 @@ from typing import Optional, Sequence
 import torch
 
 from . import _binding as _b
-from ._binding import MuonBankError, MB_MAX_BANKS  # noqa: F401
+from ._binding import MuonBankError, MB_MAX_BANKS, MB_STEP_FUSE_ROWSTATS, MB_STEP_FUSE_UPDATE  # noqa: F401
 
 __all__ = [
     "muon_bank_step", "normuon_bank_step", "muon_multi_step", "mb_workspace_bytes",
@@ -176,14 +176,20 @@ def mb_multi_workspace_bytes(banks: Sequence[BankState], normuon: bool = False) 
 
 
 def muon_multi_step(banks: Sequence[BankState], lr: float, wd: float, mu: float, normuon: bool = False,
-                    beta2: float = 0.95, ns_steps: int = 5, workspace=None, stream=None):
-    """One step over several banks as one launch sequence."""
+                    beta2: float = 0.95, ns_steps: int = 5, workspace=None, stream=None, flags: int = 0):
+    """One step over several banks as one launch sequence (flags: MB_STEP_* options, which go
+    through muon_multi_step_ex)."""
     arr = _descs(banks)
     ws = _workspace(mb_multi_workspace_bytes(banks, normuon), workspace, banks[0].bank.device)
+    lib = _b.load()
     with _on(banks[0].bank):
-        st = _b.load().muon_multi_step(arr, len(banks), lr, wd, mu, int(normuon), beta2, ns_steps, ws.data_ptr(),
-                                       ws.numel() * ws.element_size(), _stream(stream))
-    _b.check("muon_multi_step", st)
+        if flags:
+            st = lib.muon_multi_step_ex(arr, len(banks), lr, wd, mu, int(normuon), beta2, ns_steps, flags,
+                                        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+        else:
+            st = lib.muon_multi_step(arr, len(banks), lr, wd, mu, int(normuon), beta2, ns_steps, ws.data_ptr(),
+                                     ws.numel() * ws.element_size(), _stream(stream))
+    _b.check("muon_multi_step_ex" if flags else "muon_multi_step", st)
     return ws
 
 

@@ -30,6 +30,8 @@ MB_ERR_SCRATCH_LIMIT = -11
 MB_ERR_DEVICE = -12
 MB_NOALLOC_SCRATCH_BYTES = 32 << 20
 MB_MAX_BANKS = 8
+MB_STEP_FUSE_UPDATE = 1
+MB_STEP_FUSE_ROWSTATS = 2
 
 
 class MbShape(ctypes.Structure):
@@ -50,6 +52,8 @@ _SIGNATURES = {
     "mb_multi_workspace_bytes": (c_int, [ctypes.POINTER(MbBankDesc), c_int, c_int, ctypes.POINTER(c_size_t)]),
     "muon_multi_step": (c_int, [ctypes.POINTER(MbBankDesc), c_int, c_float, c_float, c_float, c_int, c_float,
                                 c_int, _P, c_size_t, _P]),
+    "muon_multi_step_ex": (c_int, [ctypes.POINTER(MbBankDesc), c_int, c_float, c_float, c_float, c_int, c_float,
+                                   c_int, c_uint, _P, c_size_t, _P]),
     "muon_multi_step_dev": (c_int, [ctypes.POINTER(MbBankDesc), c_int, _P, c_int, c_int, _P, c_size_t, _P]),
     "mb_momentum": (c_int, [_P, _P, _P, MbShape, c_float, _P]),
     "mb_newton_schulz": (c_int, [_P, _P, MbShape, c_int, _P, c_size_t, _P]),

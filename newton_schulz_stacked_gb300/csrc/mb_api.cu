@@ -172,6 +172,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Layout {
   int batch, rows, cols, m, n, tall, small, ld, ldm, P;
   size_t x[3], a, b, xf[2], partials, scale, q, rowscale;  // x[0] = u, x[1], x[2] = iterates
+  size_t rowsq;              // NorMuon, large banks: row sums of v^2 per 32-column chunk [batch][nchunk][rows]
+  int nchunk;
   size_t sync, sync_bytes;   // large banks: NS completion counters, then the task counter
   size_t dscal;              // derived scalars of a step with device-memory hyperparameters
   size_t end;
@@ -212,9 +214,11 @@ Layout make_layout(const mb_shape& s, int normuon, size_t base) {
   L.dscal = take(DSCAL_COUNT * sizeof(float));
   L.partials = take(B * L.P * 4);
   L.scale = take(B * 4);
+  L.nchunk = (s.cols + 31) / 32;
   if (normuon) {
     L.q = take(B * s.rows * 4);
     L.rowscale = take(B * s.rows * 4);
+    if (!L.small) L.rowsq = take(B * static_cast<size_t>(L.nchunk) * s.rows * 4);
   }
   L.end = align_up(off, WS_ALIGN);
   return L;
@@ -229,6 +233,9 @@ int final_buffer(int ns_steps) { return ns_steps == 0 ? 1 : iterate_buffer(ns_st
 struct Bank {
   uint16_t* bank;
   uint16_t* bank_copy;  // optional second destination of the updated bank
+  int fin = FIN_NONE;   // what the last Newton-Schulz step's epilogue does for this bank (FinMode)
+  float decay = 0.f, neg_lr = 0.f;   // S5 scalars (FIN_UPDATE)
+  const float* dscal = nullptr;      // or the derived scalars in device memory
   const uint16_t* grad;
   float* mom;
   uint16_t* mant;
@@ -453,6 +460,16 @@ int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceS
       MB_TRY(encode_map(&nb_.st_b, k.ws + L.b, L.m, L.m, L.batch, L.ldm, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
       nb_.scale = k.at<float>(L.scale);
       nb_.done = k.at<unsigned>(L.sync);
+      nb_.fin = k.fin;
+      nb_.store_v = 1;
+      nb_.w = k.bank;
+      nb_.mant = k.mant;
+      nb_.w_copy = k.bank_copy;
+      nb_.decay = k.decay;
+      nb_.neg_lr = k.neg_lr;
+      nb_.dscal = k.dscal;
+      nb_.rowsq = k.fin == FIN_ROWSQ ? k.at<float>(L.rowsq) : nullptr;
+      nb_.nchunk = L.nchunk;
       nb_.batch = L.batch;
       nb_.rows = L.rows;
       nb_.cols = L.cols;
@@ -490,18 +507,21 @@ int stage_ns_launches(const Bank* b, int nb, int steps, cudaStream_t st, DeviceS
   return MB_OK;
 }
 
-// S6 statistics: per-row factor into rowscale, state in place; v with pitch `vld`.
+// S6 statistics: per-row factor into rowscale, state in place; v with pitch `vld`.  Banks whose
+// last Newton-Schulz epilogue wrote their row sums (FIN_ROWSQ) skip the pass over v.
 int stage_normuon(const Bank* b, int nb, float beta2, const uint16_t* const* v, const int* vld, cudaStream_t st,
                   bool dev_scalars = false) {
-  RowParams rp{};
+  RowParams rp{}, sp{};
   rp.nb = nb;
-  rp.beta2 = beta2;
-  int rows = 0, mats = 0;
+  rp.beta2 = sp.beta2 = beta2;
+  int rows = 0, mats = 0, srows = 0;
   for (int i = 0; i < nb; ++i) {
     RowBank& r = rp.b[i];
     const Layout& L = b[i].L;
     r.v = v[i];
     r.q = b[i].at<float>(L.q);
+    r.rowsq = b[i].fin == FIN_ROWSQ ? b[i].at<float>(L.rowsq) : nullptr;
+    r.nchunk = L.nchunk;
     r.state = b[i].row_state;
     r.rowscale = b[i].at<float>(L.rowscale);
     r.batch = L.batch;
@@ -513,28 +533,52 @@ int stage_normuon(const Bank* b, int nb, float beta2, const uint16_t* const* v, 
     r.dscal = dev_scalars ? b[i].at<float>(L.dscal) : nullptr;
     rows += L.batch * L.rows;
     mats += L.batch;
+    if (!r.rowsq) {
+      sp.b[sp.nb] = r;
+      sp.b[sp.nb].row_begin = srows;
+      ++sp.nb;
+      srows += L.batch * L.rows;
+    }
   }
   rp.total_rows = rows;
   rp.total_mats = mats;
-  MB_LAUNCH(launch_row_sumsq(rp, st), rp.total_rows > 0, MB_MARK_ROWSTATS, st);
+  sp.total_rows = srows;
+  MB_LAUNCH(launch_row_sumsq(sp, st), sp.total_rows > 0, MB_MARK_ROWSTATS, st);
   MB_LAUNCH(launch_row_scale(rp, st), rp.total_mats > 0, MB_MARK_ROWSTATS, st);
   return MB_OK;
 }
 
-// S5: update from v (pitch vld); NorMuon uses the per-row factors.
+// S5: update from v (pitch vld); NorMuon uses the per-row factors.  Banks whose last
+// Newton-Schulz epilogue already updated them (FIN_UPDATE) are left out.
 // sqrt(max(1, rows / cols)): the shape factor of the learning rate ("Muon Custom Sizing", section 4).
 double shape_factor(const Layout& L) { return std::sqrt(std::fmax(1.0, static_cast<double>(L.rows) / L.cols)); }
 
-int stage_k3(const Bank* b, int nb, bool normuon, float lr, float wd, const uint16_t* const* v, const int* vld,
-             cudaStream_t st, bool dev_scalars = false) {
+// 1 - lr*wd (rounded once) and -lr*sqrt(max(1, rows/cols)), formed in double and rounded to fp32.
+void update_scalars(float lr, float wd, const Layout& L, float* decay, float* neg_lr) {
+  const double lrd = lr, wdd = wd;
+  *decay = static_cast<float>(std::fma(-lrd, wdd, 1.0));
+  *neg_lr = static_cast<float>(-lrd * shape_factor(L));
+}
+
+int stage_k3(const Bank* b_all, int nb_all, bool normuon, float lr, float wd, const uint16_t* const* v_all,
+             const int* vld_all, cudaStream_t st, bool dev_scalars = false) {
+  Bank b[MAX_BANKS];
+  const uint16_t* v[MAX_BANKS];
+  int vld[MAX_BANKS], nb = 0;
+  for (int i = 0; i < nb_all; ++i) {
+    if (b_all[i].fin == FIN_UPDATE) continue;
+    b[nb] = b_all[i];
+    v[nb] = v_all[i];
+    vld[nb] = vld_all[i];
+    ++nb;
+  }
+  if (nb == 0) return MB_OK;
   EwParams p = ew_params(b, nb, [&](const Bank& k, EwBank& e) {
     e.bank = k.bank;
     e.bank_copy = k.bank_copy;
     e.mant = k.mant;
     e.rowscale = normuon ? k.at<float>(k.L.rowscale) : nullptr;
-    const double lrd = lr, wdd = wd;
-    e.decay = static_cast<float>(std::fma(-lrd, wdd, 1.0));   // 1 - lr*wd, rounded once
-    e.neg_lr = static_cast<float>(-lrd * shape_factor(k.L));
+    update_scalars(lr, wd, k.L, &e.decay, &e.neg_lr);
     e.dscal = dev_scalars ? k.at<float>(k.L.dscal) : nullptr;
   });
   for (int i = 0; i < nb; ++i) {
@@ -543,6 +587,17 @@ int stage_k3(const Bank* b, int nb, bool normuon, float lr, float wd, const uint
   }
   MB_LAUNCH(launch_k3(p, normuon, st), p.total_blocks > 0, MB_MARK_UPDATE, st);
   return MB_OK;
+}
+
+// What the last Newton-Schulz step's epilogue of a bank does in a whole step, as the call's
+// MB_STEP_* flags ask: with NorMuon, sum v^2 per row (MB_STEP_FUSE_ROWSTATS); without, apply
+// the update itself (MB_STEP_FUSE_UPDATE, rows of whole 16-byte pieces).  Neither for the fp32
+// small-matrix path, nor with fewer than 3 steps (the first two steps' APPLY epilogues carry the
+// first iterate's residual).
+int fin_mode(const Layout& L, int ns_steps, int normuon, unsigned flags) {
+  if (L.small || ns_steps < 3) return FIN_NONE;
+  if (normuon) return (flags & MB_STEP_FUSE_ROWSTATS) ? FIN_ROWSQ : FIN_NONE;
+  return ((flags & MB_STEP_FUSE_UPDATE) && L.cols % 8 == 0) ? FIN_UPDATE : FIN_NONE;
 }
 
 // ---------------------------------------------------------------- whole step
@@ -592,8 +647,9 @@ int check_workspace(void* ws, size_t have, size_t need) {
 // device memory when the step runs ({lr, wd, mu, beta2} per bank) and lr..beta2
 // are ignored.
 int run_step(const mb_bank_desc* d, int nb, float lr, float wd, float mu, int normuon, float beta2, int ns_steps,
-             void* workspace, size_t ws_bytes, void* stream, const float* scalars_dev = nullptr) {
+             void* workspace, size_t ws_bytes, void* stream, const float* scalars_dev = nullptr, unsigned flags = 0) {
   if (!d) return MB_ERR_NULL;
+  if (flags & ~static_cast<unsigned>(MB_STEP_FUSE_UPDATE | MB_STEP_FUSE_ROWSTATS)) return MB_ERR_ARG;
   if (nb <= 0 || nb > MAX_BANKS) return nb <= 0 ? MB_ERR_ARG : MB_ERR_TOO_MANY;
   if (ns_steps < 0 || ns_steps > MAX_NS_STEPS) return MB_ERR_NS_STEPS;
   const bool dev = scalars_dev != nullptr;
@@ -618,6 +674,9 @@ int run_step(const mb_bank_desc* d, int nb, float lr, float wd, float mu, int no
     b[i].row_state = d[i].row_state;
     b[i].L = L[i];
     b[i].ws = static_cast<uint8_t*>(workspace);
+    b[i].fin = fin_mode(L[i], ns_steps, normuon, flags);
+    update_scalars(lr, wd, L[i], &b[i].decay, &b[i].neg_lr);
+    b[i].dscal = dev ? b[i].at<float>(L[i].dscal) : nullptr;
     v[i] = b[i].at<uint16_t>(L[i].x[final_buffer(ns_steps)]);
     vld[i] = L[i].ld;
   }
@@ -736,6 +795,13 @@ int muon_multi_step(const mb_bank_desc* banks, int n_banks, float lr, float wd, 
                     float beta2, int ns_steps, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return run_step(banks, n_banks, lr, wd, mu, normuon ? 1 : 0, beta2, ns_steps, workspace, workspace_bytes,
                   cuda_stream);
+}
+
+int muon_multi_step_ex(const mb_bank_desc* banks, int n_banks, float lr, float wd, float mu, int normuon,
+                       float beta2, int ns_steps, unsigned flags, void* workspace, size_t workspace_bytes,
+                       void* cuda_stream) {
+  return run_step(banks, n_banks, lr, wd, mu, normuon ? 1 : 0, beta2, ns_steps, workspace, workspace_bytes,
+                  cuda_stream, nullptr, flags);
 }
 
 int muon_multi_step_dev(const mb_bank_desc* banks, int n_banks, const float* scalars_dev, int normuon,

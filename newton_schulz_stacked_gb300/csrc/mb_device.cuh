@@ -394,4 +394,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return float_to_bf16_bits(lo) | (float_to_bf16_bits(hi) << 16);
 }
 
+// S5 on one element (Track-2 record 7 write-up, section 4.1): the fp32 weight is the bf16
+// bits (high half) and the mantissa (low half); decay and step are two separately rounded
+// products and one rounded sum (no contraction); the result splits back by truncation.
+__device__ __forceinline__ void update_one(uint32_t& w16, uint32_t& m16, float v, float decay, float neg_lr) {
+  const float w = __uint_as_float((w16 << 16) | m16);
+  const float r = __fadd_rn(__fmul_rn(w, decay), __fmul_rn(neg_lr, v));
+  const uint32_t bits = __float_as_uint(r);
+  w16 = bits >> 16;
+  m16 = bits & 0xFFFFu;
+}
+
+// Eight consecutive elements of S5: bank bits w8, mantissa m8 (eight 16-bit values each,
+// packed two per word), v8 the bf16 update bits; returns the new bank bits in w8, mantissa in m8.
+__device__ __forceinline__ void update_eight(uint4& w8, uint4& m8, const uint4& v8, float decay, float neg_lr) {
+  uint32_t w[4] = {w8.x, w8.y, w8.z, w8.w}, m[4] = {m8.x, m8.y, m8.z, m8.w};
+  const uint32_t v[4] = {v8.x, v8.y, v8.z, v8.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w0 = w[i] & 0xFFFFu, w1 = w[i] >> 16, m0 = m[i] & 0xFFFFu, m1 = m[i] >> 16;
+    update_one(w0, m0, bf16_bits_to_float(v[i] & 0xFFFFu), decay, neg_lr);
+    update_one(w1, m1, bf16_bits_to_float(v[i] >> 16), decay, neg_lr);
+    w[i] = w0 | (w1 << 16);
+    m[i] = m0 | (m1 << 16);
+  }
+  w8 = make_uint4(w[0], w[1], w[2], w[3]);
+  m8 = make_uint4(m[0], m[1], m[2], m[3]);
+}
+
 }  // namespace mb

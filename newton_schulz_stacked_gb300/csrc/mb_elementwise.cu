@@ -330,7 +330,16 @@ __global__ void __launch_bounds__(256) row_scale_kernel(const __grid_constant__ 
   const float b2 = beta2, omb2 = 1.0f - beta2;
   float nv = 0.f, nh = 0.f;
   for (int r = threadIdx.x; r < B.rows; r += 256) {
-    const float q = B.q[base + r];
+    float q;
+    if (B.rowsq) {
+      // the row's sums over its 32-column chunks, written by the Newton-Schulz epilogue, in chunk order
+      const float* rq = B.rowsq + static_cast<size_t>(mat) * B.nchunk * B.rows + r;
+      q = 0.f;
+      for (int c = 0; c < B.nchunk; ++c) q += rq[static_cast<size_t>(c) * B.rows];
+      B.q[base + r] = q;
+    } else {
+      q = B.q[base + r];
+    }
     const float s = fmaf(b2, B.state[base + r], omb2 * (q * inv_cols));
     B.state[base + r] = s;
     const float d = fmaxf(s, NORMUON_FLOOR);
@@ -364,14 +373,6 @@ __global__ void __launch_bounds__(256) row_scale_kernel(const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------- S5 update
-
-__device__ __forceinline__ void update_one(uint32_t& w16, uint32_t& m16, float v, float decay, float neg_lr) {
-  const float w = __uint_as_float((w16 << 16) | m16);
-  const float r = __fadd_rn(__fmul_rn(w, decay), __fmul_rn(neg_lr, v));
-  const uint32_t bits = __float_as_uint(r);
-  w16 = bits >> 16;
-  m16 = bits & 0xFFFFu;
-}
 
 template <bool NORMUON>
 __global__ void __launch_bounds__(EW_THREADS) k3_kernel(const __grid_constant__ EwParams p) {

@@ -90,6 +90,8 @@ struct SmallParams {
 struct RowBank {
   const uint16_t* v;    // NS output, pitch ld
   float* q;             // per-row sum of v^2 [batch * rows]
+  const float* rowsq;   // or, from the Newton-Schulz epilogue: sums per 32-column chunk [batch][nchunk][rows]
+  int nchunk;
   float* state;         // row second moment [batch * rows] (in place)
   float* rowscale;      // per-row factor [batch * rows]
   int batch, rows, cols, ld;
@@ -106,6 +108,13 @@ struct RowParams {
 // ---------------------------------------------------------------- Newton-Schulz GEMMs
 
 enum GemmEpi { EPI_GRAM = 0, EPI_POLY = 1, EPI_APPLY = 2 };   // the three GEMM phases of one step
+
+// What the last step's APPLY epilogue of a bank does beyond storing v:
+//   FIN_UPDATE  S5 on the output in place: the bank and mantissa (and the optional bank copy)
+//               are read, updated with the bf16-rounded v and written back by that epilogue;
+//   FIN_ROWSQ   NorMuon: the sums of v^2 of each row over each 32-column chunk, per matrix,
+//               into rowsq [batch][nchunk][rows] (chunk-major), for the row-scale kernel.
+enum FinMode { FIN_NONE = 0, FIN_UPDATE = 1, FIN_ROWSQ = 2 };
 
 constexpr int MAX_NS_BANKS = 4;     // large banks per fused Newton-Schulz launch
 
@@ -125,6 +134,15 @@ struct NsBank {
   int batch, rows, cols, m, n, tall;
   int T, sym_pairs;                 // 128-blocks per side of A; pair tasks per matrix of GRAM and POLY
   int tn, apply_pairs;              // 256-wide column tiles and pair tasks per matrix of APPLY
+  // the last step's APPLY epilogue (FinMode); FIN_UPDATE needs cols % 8 == 0 (16-byte row pieces)
+  int fin, store_v;                 // store_v = 0: the last APPLY writes no v (FIN_UPDATE only)
+  uint16_t* w;                      // FIN_UPDATE: bank bf16 bits [batch, rows, cols], in place
+  uint16_t* mant;                   //             mantissa, in place
+  uint16_t* w_copy;                 //             optional second destination of the bank, or null
+  float decay, neg_lr;              //             1 - lr*wd, -lr*sqrt(max(1, rows/cols))
+  const float* dscal;               //             derived scalars in device memory, or null
+  float* rowsq;                     // FIN_ROWSQ: [batch][nchunk][rows] partial sums of v^2
+  int nchunk;                       //            ceil(cols / 32)
 };
 
 struct NsParams {
@@ -156,6 +174,7 @@ cudaError_t launch_row_scale(const RowParams& p, cudaStream_t s);
 cudaError_t launch_k3(const EwParams& p, bool normuon, cudaStream_t s);
 cudaError_t launch_scalars(const ScalarParams& p, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
-cudaError_t launch_ns_fused(const NsParams& p, cudaStream_t s);
+cudaError_t launch_ns_fused(const NsParams& p, cudaStream_t s);       // plain or with FinModes, as the banks ask
+cudaError_t launch_ns_fused_fin(const NsParams& p, cudaStream_t s);   // the instantiation with FinModes
 
 }  // namespace mb

@@ -180,6 +180,12 @@ def test_multi_step_argument_errors(lib):
     assert lib.muon_multi_step_dev(arr, 9, good, 0, 5, good, 1 << 30, None) == b.MB_ERR_TOO_MANY
     assert lib.muon_multi_step_dev(arr, 2, good, 0, 17, good, 1 << 30, None) == b.MB_ERR_NS_STEPS
     assert lib.muon_multi_step_dev(arr, 2, good, 1, 5, good, 1 << 30, None) == b.MB_ERR_NULL
+    # options: unknown bits are refused; the known ones pass the argument checks (and then
+    # meet the bad workspace size like the plain call)
+    assert lib.muon_multi_step_ex(arr, 2, 0.02, 0.01, 0.95, 0, 0.95, 5, 4, good, 1 << 62, None) == b.MB_ERR_ARG
+    for flags in (b.MB_STEP_FUSE_UPDATE, b.MB_STEP_FUSE_ROWSTATS, 3):
+        assert lib.muon_multi_step_ex(arr, 2, 0.02, 0.01, 0.95, 0, 0.95, 5, flags, good, 16, None) == \
+            b.MB_ERR_WORKSPACE
 
 
 def test_stage_argument_errors(lib):

@@ -262,6 +262,64 @@ def test_normuon_update_stage(nss, beta2):
     assert check_update(w, mant, v, u16(wt), u16(mt), LR, WD, shape[1], shape[2], vhat=vhat) <= UPDATE_TOL
 
 
+# the default step and the step with the update fused into the last Newton-Schulz epilogue
+# (large banks whose columns are a multiple of 8, at least 3 steps; the separate update kernel
+# for the rest) give the same bits as the stage calls
+@pytest.mark.parametrize("fuse", [False, True])
+@pytest.mark.parametrize("shape,ns_steps", [((3, 256, 384), 5), ((2, 384, 256), 5), ((2, 200, 328), 5),
+                                            ((1, 768, 3072), 5), ((2, 3072, 768), 5), ((2, 256, 384), 3),
+                                            ((2, 256, 384), 2), ((2, 200, 330), 5), ((3, 300, 520), 4)])
+def test_step_equals_its_stage_calls(nss, shape, ns_steps, fuse):
+    """A whole step gives the same bits as the same step run as separate stage calls (momentum,
+    Newton-Schulz, the update kernel), the bank copy included."""
+    w, mant, mom, _, g = _case(70 + ns_steps, shape, std=1e-3)
+    a = nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant), None, torch.zeros_like(to_dev(w)))
+    nss.muon_multi_step([a], LR, WD, MU, ns_steps=ns_steps, flags=nss.MB_STEP_FUSE_UPDATE if fuse else 0)
+    gt, mt, wt, at = to_dev(g), to_dev(mom), to_dev(w), to_dev(mant)
+    ut, vt = torch.empty_like(gt), torch.empty_like(gt)
+    nss.mb_momentum(gt, mt, ut, MU)
+    nss.mb_newton_schulz(ut, vt, ns_steps=ns_steps)
+    nss.mb_update(wt, at, vt, LR, WD)
+    torch.cuda.synchronize()
+    assert nss.mb_sync_status() == 0
+    np.testing.assert_array_equal(f32(a.momentum), f32(mt))
+    np.testing.assert_array_equal(u16(a.bank), u16(wt))
+    np.testing.assert_array_equal(u16(a.mantissa), u16(at))
+    np.testing.assert_array_equal(u16(a.bank_copy), u16(wt))
+
+
+@pytest.mark.parametrize("fuse", [False, True])
+def test_normuon_multi_step_mixed_banks(nss, fuse):
+    """NorMuon over tensor-core banks and an fp32 gate bank in one call, with the tensor-core
+    banks' row sums from their own pass or from the last Newton-Schulz epilogue (the gate bank's
+    always from the pass, ragged 328-column rows included): every bank's row state and update
+    against the oracle given the GPU's v."""
+    shapes = [(3, 256, 384), (4, 6, 12), (2, 200, 328)]
+    states = [_case(90 + i, s) for i, s in enumerate(shapes)]
+    banks = [nss.BankState(to_dev(w), to_dev(g), to_dev(mom), to_dev(mant), to_dev(row))
+             for (w, mant, mom, row, g) in states]
+    ws = torch.empty(nss.mb_multi_workspace_bytes(banks, True), dtype=torch.uint8, device="cuda:0")
+    nss.muon_multi_step(banks, LR, WD, MU, normuon=True, beta2=0.95, ns_steps=5, workspace=ws,
+                        flags=nss.MB_STEP_FUSE_ROWSTATS if fuse else 0)
+    torch.cuda.synchronize()
+    assert nss.mb_sync_status() == 0
+    off = 0
+    for (w, mant, mom, row, g), b, shape in zip(states, banks, shapes):
+        B, R, C = shape
+        u_off, v_off, pitch = nss.mb_workspace_views(shape, normuon=True)
+        v_gpu = ws_matrix(ws, off + v_off, shape, pitch)
+        u_gpu = ws_matrix(ws, off + u_off, shape, pitch)
+        off += nss.mb_workspace_bytes(shape, True)
+        assert check_ns(u_gpu, v_gpu).max() <= ns_tol(R, C)
+        state = f32(b.row_state)
+        vhat = []
+        for k in range(B):
+            vh, st = O.normuon(O.bf16_bits_to_f64(v_gpu[k]), row[k], 0.95)
+            assert O.rel_frobenius(state[k], st) <= STATE_TOL, (shape, k)
+            vhat.append(vh)
+        assert check_update(w, mant, v_gpu, u16(b.bank), u16(b.mantissa), LR, WD, R, C, vhat=vhat) <= UPDATE_TOL
+
+
 def test_multi_step_equals_single_steps(nss):
     shapes = [(8, 256, 256), (6, 512, 256), (1, 12, 768), (10, 6, 12)]
     states = [_case(30 + i, s, dead=((5,) if i == 1 else ())) for i, s in enumerate(shapes)]
