@@ -132,6 +132,23 @@ def test_newton_schulz(nss, shape, kind):
     assert errs.max() <= ns_tol(*shape[1:]), errs
 
 
+# one matrix for every count T of 128-blocks per side of A from 2 to 17: T = 3 .. 16 take their
+# GRAM and POLY tasks from the table covers of the block pairs, 2 and 17 the plain 2 x 2 tiling;
+# the last block is ragged, and wide and tall slices alternate
+@pytest.mark.parametrize("T", range(2, 18))
+def test_newton_schulz_every_block_count(nss, T):
+    m = 128 * T - 50
+    shape = (1, m, m + 72) if T % 2 else (1, m + 72, m)
+    u = synth.to_bf16_bits(np.random.default_rng(500 + T).standard_normal(shape))
+    ut = to_dev(u)
+    vt = torch.empty_like(ut)
+    nss.mb_newton_schulz(ut, vt, ns_steps=5)
+    torch.cuda.synchronize()
+    assert nss.mb_sync_status() == 0
+    errs = check_ns(u, u16(vt))
+    assert errs.max() <= ns_tol(*shape[1:]), errs
+
+
 @pytest.mark.parametrize("steps", [0, 1, 2, 3, 8, 16])   # 16: the most one call accepts
 @pytest.mark.parametrize("shape", [(2, 256, 384), (2, 384, 256), (2, 12, 40)])
 def test_newton_schulz_steps(nss, steps, shape):
