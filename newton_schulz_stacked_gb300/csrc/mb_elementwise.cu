@@ -4,7 +4,8 @@
 //   k1_kernel      S1 momentum (lerp form, "Muon Custom Sizing" write-up,
 //                  section 4) writing u in bf16, plus per-chunk sums of u^2
 //                  for the Frobenius normalisation (S2).  128-bit loads and
-//                  stores, warp-shuffle block reductions in a fixed order.
+//                  stores, warp-shuffle reductions in a fixed order; the
+//                  arithmetic is the warp units of mb_ew_units.cuh.
 //   scale_kernel   s = 1/(||u||_F + 1e-7) per matrix from those partial sums.
 //   small_ns       the quintic iteration (same write-up, section 2.3) in fp32
 //                  for matrices with min(rows, cols) <= 64.
@@ -16,6 +17,7 @@
 #include <atomic>
 
 #include "mb_device.cuh"
+#include "mb_ew_units.cuh"
 #include "mb_internal.h"
 
 namespace mb {
@@ -31,25 +33,11 @@ __device__ __forceinline__ int ew_bank(const EwParams& p) {
   return bi;
 }
 
-// Fixed-order block sum (EW_THREADS threads); result valid in thread 0.
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < EW_THREADS / 32; ++w) t += red[w];
-  }
-  return t;
-}
-
 // ---------------------------------------------------------------- S1 (+ S2 partials)
 
 template <bool MOMENTUM>
 __global__ void __launch_bounds__(EW_THREADS) k1_kernel(const __grid_constant__ EwParams p) {
-  __shared__ float red[EW_THREADS / 32];
+  __shared__ float red[EW_UNITS_PER_CHUNK];
   const EwBank& B = p.b[ew_bank(p)];
   const int local = blockIdx.x - B.block_begin;
   const int mat = local / B.P, chunk = local - mat * B.P;
@@ -57,81 +45,19 @@ __global__ void __launch_bounds__(EW_THREADS) k1_kernel(const __grid_constant__ 
   const int e0 = chunk * EW_CHUNK;
   const int e1 = min(E, e0 + EW_CHUNK);
   const size_t moff = static_cast<size_t>(mat) * E;
-  const uint16_t* src = B.src + moff;
-  float* mom = MOMENTUM ? B.mom + moff : nullptr;
-  uint16_t* xo = B.xout + static_cast<size_t>(mat) * B.rows * B.out_ld;
   const float mu = B.dscal ? B.dscal[DSCAL_MU] : p.mu, omm = B.dscal ? B.dscal[DSCAL_OMM] : p.omm;
-  float ss = 0.f;
-
-  auto step = [&](float g, float& b) -> float {
-    if (!MOMENTUM) return g;
-    const float bn = fmaf(omm, g - b, b);  // lerp(buf, g, 1 - mu)
-    b = bn;
-    return fmaf(mu, bn - g, g);            // lerp(g, buf_new, mu)
-  };
-
-  if ((B.cols & 7) == 0) {
-    // every load of the thread's part of the chunk first (they may not move past the u
-    // stores, which could alias the gradient), then the arithmetic and stores in element order
-    constexpr int SLICES = EW_CHUNK / (EW_THREADS * 8);
-    uint4 gl[SLICES];
-    float4 ml[SLICES][2];
-#pragma unroll
-    for (int j = 0; j < SLICES; ++j) {
-      const int e = e0 + (j * EW_THREADS + static_cast<int>(threadIdx.x)) * 8;
-      if (e < e1) {
-        gl[j] = *reinterpret_cast<const uint4*>(src + e);
-        if (MOMENTUM) {
-          ml[j][0] = *reinterpret_cast<const float4*>(mom + e);
-          ml[j][1] = *reinterpret_cast<const float4*>(mom + e + 4);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < SLICES; ++j) {
-      const int e = e0 + (j * EW_THREADS + static_cast<int>(threadIdx.x)) * 8;
-      if (e >= e1) break;
-      const int row = e / B.cols, col = e - row * B.cols;
-      const uint32_t gw[4] = {gl[j].x, gl[j].y, gl[j].z, gl[j].w};
-      float bm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (MOMENTUM) {
-        bm[0] = ml[j][0].x; bm[1] = ml[j][0].y; bm[2] = ml[j][0].z; bm[3] = ml[j][0].w;
-        bm[4] = ml[j][1].x; bm[5] = ml[j][1].y; bm[6] = ml[j][1].z; bm[7] = ml[j][1].w;
-      }
-      uint32_t uw[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float g0 = bf16_bits_to_float(gw[i] & 0xFFFFu);
-        const float g1 = bf16_bits_to_float(gw[i] >> 16);
-        const float u0 = step(g0, bm[2 * i]);
-        const float u1 = step(g1, bm[2 * i + 1]);
-        const uint32_t b0 = float_to_bf16_bits(u0), b1 = float_to_bf16_bits(u1);
-        const float r0 = bf16_bits_to_float(b0), r1 = bf16_bits_to_float(b1);
-        ss = fmaf(r0, r0, ss);
-        ss = fmaf(r1, r1, ss);
-        uw[i] = b0 | (b1 << 16);
-      }
-      if (MOMENTUM) {
-        *reinterpret_cast<float4*>(mom + e) = make_float4(bm[0], bm[1], bm[2], bm[3]);
-        *reinterpret_cast<float4*>(mom + e + 4) = make_float4(bm[4], bm[5], bm[6], bm[7]);
-      }
-      *reinterpret_cast<uint4*>(xo + static_cast<size_t>(row) * B.out_ld + col) =
-          make_uint4(uw[0], uw[1], uw[2], uw[3]);
-    }
-  } else {
-    for (int e = e0 + threadIdx.x; e < e1; e += EW_THREADS) {
-      const int row = e / B.cols, col = e - row * B.cols;
-      float b = MOMENTUM ? mom[e] : 0.f;
-      const float u = step(bf16_bits_to_float(src[e]), b);
-      if (MOMENTUM) mom[e] = b;
-      const uint32_t ub = float_to_bf16_bits(u);
-      const float r = bf16_bits_to_float(ub);
-      ss = fmaf(r, r, ss);
-      xo[static_cast<size_t>(row) * B.out_ld + col] = static_cast<uint16_t>(ub);
-    }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // each warp is one unit of the chunk; the chunk's sum of u^2 adds the units' in warp order
+  const float ss = momentum_unit<MOMENTUM>(B.src + moff, MOMENTUM ? B.mom + moff : nullptr,
+                                           B.xout + static_cast<size_t>(mat) * B.rows * B.out_ld, B.cols, B.out_ld,
+                                           e0, e1, w, lane, mu, omm);
+  if (lane == 0) red[w] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0 && B.partials) {
+    float t = 0.f;
+    for (int i = 0; i < EW_UNITS_PER_CHUNK; ++i) t += red[i];
+    B.partials[static_cast<size_t>(mat) * B.P + chunk] = t;
   }
-  const float tot = block_sum(ss, red);
-  if (threadIdx.x == 0 && B.partials) B.partials[static_cast<size_t>(mat) * B.P + chunk] = tot;
 }
 
 // ---------------------------------------------------------------- S2 finalise
@@ -144,12 +70,8 @@ __global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ Scal
   while (bi + 1 < p.nb && gm >= p.b[bi + 1].mat_begin) ++bi;
   const ScaleBank& B = p.b[bi];
   const int mat = gm - B.mat_begin;
-  const float* part = B.partials + static_cast<size_t>(mat) * B.P;
-  float t = 0.f;
-  for (int i = lane; i < B.P; i += 32) t += part[i];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-  if (lane == 0) B.scale[mat] = 1.0f / (sqrtf(t) + NS_EPS);
+  const float s = scale_from_units(B.partials + static_cast<size_t>(mat) * B.P, B.P, lane);
+  if (lane == 0) B.scale[mat] = s;
 }
 
 // ns_steps == 0: v = bf16(s * u)
@@ -382,51 +304,12 @@ __global__ void __launch_bounds__(EW_THREADS) k3_kernel(const __grid_constant__ 
   const int E = B.rows * B.cols;
   const int e0 = chunk * EW_CHUNK, e1 = min(E, e0 + EW_CHUNK);
   const size_t moff = static_cast<size_t>(mat) * E;
-  uint16_t* wb = B.bank + moff;
-  uint16_t* mb_ = B.mant + moff;
-  uint16_t* wc = B.bank_copy ? B.bank_copy + moff : nullptr;
-  const uint16_t* v = B.xin + static_cast<size_t>(mat) * B.rows * B.ld;
-  const float* rs = NORMUON ? B.rowscale + static_cast<size_t>(mat) * B.rows : nullptr;
   const float decay = B.dscal ? B.dscal[DSCAL_DECAY] : B.decay;
   const float neg_lr = B.dscal ? B.dscal[DSCAL_NEG_LR] : B.neg_lr;
-  if ((B.cols & 7) == 0) {
-    for (int e = e0 + threadIdx.x * 8; e < e1; e += EW_THREADS * 8) {
-      const int row = e / B.cols, col = e - row * B.cols;
-      const uint4 wv = *reinterpret_cast<const uint4*>(wb + e);
-      const uint4 mv = *reinterpret_cast<const uint4*>(mb_ + e);
-      const uint4 vv = *reinterpret_cast<const uint4*>(v + static_cast<size_t>(row) * B.ld + col);
-      const float f = NORMUON ? rs[row] : 1.0f;
-      uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w}, m[4] = {mv.x, mv.y, mv.z, mv.w};
-      const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t w0 = w[i] & 0xFFFFu, w1 = w[i] >> 16, m0 = m[i] & 0xFFFFu, m1 = m[i] >> 16;
-        float v0 = bf16_bits_to_float(vw[i] & 0xFFFFu), v1 = bf16_bits_to_float(vw[i] >> 16);
-        if (NORMUON) {
-          v0 = __fmul_rn(v0, f);
-          v1 = __fmul_rn(v1, f);
-        }
-        update_one(w0, m0, v0, decay, neg_lr);
-        update_one(w1, m1, v1, decay, neg_lr);
-        w[i] = w0 | (w1 << 16);
-        m[i] = m0 | (m1 << 16);
-      }
-      *reinterpret_cast<uint4*>(wb + e) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(mb_ + e) = make_uint4(m[0], m[1], m[2], m[3]);
-      if (wc) *reinterpret_cast<uint4*>(wc + e) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  } else {
-    for (int e = e0 + threadIdx.x; e < e1; e += EW_THREADS) {
-      const int row = e / B.cols, col = e - row * B.cols;
-      uint32_t w = wb[e], m = mb_[e];
-      float vf = bf16_bits_to_float(v[static_cast<size_t>(row) * B.ld + col]);
-      if (NORMUON) vf = __fmul_rn(vf, rs[row]);
-      update_one(w, m, vf, decay, neg_lr);
-      wb[e] = static_cast<uint16_t>(w);
-      mb_[e] = static_cast<uint16_t>(m);
-      if (wc) wc[e] = static_cast<uint16_t>(w);
-    }
-  }
+  update_unit<NORMUON>(B.bank + moff, B.mant + moff, B.bank_copy ? B.bank_copy + moff : nullptr,
+                       B.xin + static_cast<size_t>(mat) * B.rows * B.ld,
+                       NORMUON ? B.rowscale + static_cast<size_t>(mat) * B.rows : nullptr, B.cols, B.ld, e0, e1,
+                       threadIdx.x >> 5, threadIdx.x & 31, decay, neg_lr);
 }
 
 // ---------------------------------------------------------------- failure-detection self test
