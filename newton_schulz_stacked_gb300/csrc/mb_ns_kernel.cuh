@@ -5,12 +5,14 @@
 //
 // One quintic step ("Muon Custom Sizing" write-up, section 2.3; Track-2
 // record 7 write-up, section 4.2) is three GEMM phases per matrix:
-//   GRAM   A  = alpha * X X^T       (alpha = s^2 on the first step, s = 1/(||u||+eps))
-//   POLY   B  = b A + c A A         (A symmetric, so A A = A A^T)
-//   APPLY  X' = beta (a X + B X)    (beta = s on the first step)
-// A tall slice (rows > cols) stays in its stored orientation and runs the
-// swapped-operand form A = X^T X, X' = beta (a X + X B); the difference is
-// only which operand tiles are K-major and which are MN-major.
+//   GRAM   A  = alpha * X X^T         (alpha = s^2 on the first step, s = 1/(||u||+eps))
+//   POLY   B' = a I + b A + c A A     (A symmetric, so A A = A A^T)
+//   APPLY  X' = beta B' X             (beta = s on the first step)
+// so that a X + b A X + c A^2 X needs no X in APPLY's epilogue: a I rides in the stored bf16
+// B'.  The second step also adds a times the first iterate's bf16 residual (stored by the
+// first step's APPLY), so that its a X term sees X_1 to ~16 bits.  A tall slice (rows > cols)
+// stays in its stored orientation and runs the swapped-operand form A = X^T X,
+// X' = beta X B'; the difference is only which operand tiles are K-major and which MN-major.
 //
 // CTA pairs.  The kernel runs in clusters of two CTAs (one per SM) that compute
 // one 256 x nt output tile (nt = 128 or 256) with M = 256 tcgen05 MMAs
@@ -269,7 +271,7 @@ struct EpiJob {
 };
 
 // LO (APPLY only): 0 plain; LO_WRITE also stores the bf16 residual of the output (first
-// step); LO_READ adds the residual stored by the first step to its a*X term (second step).
+// step); LO_READ adds a times the residual stored by the first step (second step).
 constexpr int LO_WRITE = 1, LO_READ = 2;
 
 // Non-blocking: whether the phase with the given parity has completed (acquire at cluster scope).
@@ -286,25 +288,21 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 }
 
 // Where one epilogue warp's input of a task comes from: chunk c is the 32x32 box at
-// (col0 + 32 c, row0) of matrix `mat` of A (POLY) or X (APPLY), read through the map that
-// the phase which wrote it stored with (64-byte swizzle, so a lane reading its own row of
-// the box hits distinct banks).  Boxes reaching past the matrix read zeros.
+// (col0 + 32 c, row0) of matrix `mat` of A (POLY) or of X_1's residual (the second step's
+// APPLY), read through the map it was stored with (64-byte swizzle, so a lane reading its
+// own row of the box hits distinct banks).  GRAM and the other APPLY steps read none (nch 0).
+// Boxes reaching past the matrix read zeros.
 struct InSrc {
   const CUtensorMap* map;
-  const CUtensorMap* map2;   // the second step of APPLY: X_1's residual, chunk for chunk after X
-  int row0, col0, mat, nch, nstr;
-  __device__ __forceinline__ int units() const { return nch * nstr; }
+  int row0, col0, mat, nch;
+  __device__ __forceinline__ int units() const { return nch; }
 };
 
 __device__ __forceinline__ InSrc input_of(const NsParams& P, const Task& tk, int row_base, int half) {
-  InSrc s{nullptr, nullptr, 0, 0, 0, 0, 1};
-  if (tk.t < 0 || tk.ph == EPI_GRAM) return s;
+  InSrc s{nullptr, 0, 0, 0, 0};
+  if (tk.t < 0 || tk.ph == EPI_GRAM || (tk.ph == EPI_APPLY && tk.it != 1)) return s;
   const NsBank& B = P.bank[tk.bi];
-  s.map = tk.ph == EPI_POLY ? &B.st_a : &B.st_x[iterate_buffer(tk.it)];
-  if (tk.ph == EPI_APPLY && tk.it == 1) {
-    s.map2 = &B.st_x[2];
-    s.nstr = 2;
-  }
+  s.map = tk.ph == EPI_POLY ? &B.st_a : &B.st_x[2];
   s.row0 = tk.m0 + row_base;
   s.col0 = tk.n0 + half * (tk.nt >> 1);
   s.mat = tk.mat;
@@ -331,14 +329,12 @@ struct InFeed {
   int row_base, half;      // this warp's rows (CTA rank and quadrant) and column half
 };
 
-// Unit u of a task's input: chunk u / nstr of stream u % nstr (X, then X_1's residual).
+// Unit (chunk) u of a task's input.
 __device__ __forceinline__ void in_issue(InFeed& F, const InSrc& s, int u, int lane) {
   if (lane == 0) {
     const uint32_t slot = F.issued % IN_SLOTS;
-    const int c = s.nstr == 2 ? (u >> 1) : u;
-    const CUtensorMap* map = (s.nstr == 2 && (u & 1)) ? s.map2 : s.map;
     mbar_expect_tx(&F.full[slot], IN_BOX_BYTES);
-    tma_load_3d(F.buf + slot * IN_BOX_BYTES, map, &F.full[slot], s.col0 + 32 * c, s.row0, s.mat);
+    tma_load_3d(F.buf + slot * IN_BOX_BYTES, s.map, &F.full[slot], s.col0 + 32 * u, s.row0, s.mat);
   }
   ++F.issued;
 }
@@ -390,8 +386,8 @@ template <int EPI, int LO>
 __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uint32_t tacc, int quad, int half,
                                          int lane, uint8_t* ebuf, InFeed& F, const volatile int* abort_flag,
                                          int fin = FIN_NONE) {
-  constexpr bool has_ein = EPI != EPI_GRAM;
-  constexpr bool with_lo = EPI == EPI_APPLY && LO == LO_READ;
+  // the input: A in POLY (for b A), X_1's residual in the second step's APPLY (for a X_1)
+  constexpr bool has_ein = EPI == EPI_POLY || (EPI == EPI_APPLY && LO == LO_READ);
   uint8_t* bufD = ebuf;          // [32 rows][32 cols] bf16, 64-byte swizzle
   uint8_t* bufT = ebuf + 2048;   // [32 cols][32 rows] bf16, 64-byte swizzle (or the residual)
   const int row0 = J.m0 + quad * 32;
@@ -431,10 +427,10 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
 
     float rs[4];   // FIN_ROWSQ: sums of squares of rows 16g + lane/4 (rs[2g]) and 16g + 8 + lane/4 (rs[2g + 1])
 
-    // this chunk's input (and, in the second step's APPLY, X_1's residual), both row halves,
-    // taken into registers at the chunk's start so that its slots refill under the chunk's
-    // work; register 8g + 4p + i holds matrix i of column pair p of row half g
-    uint32_t ex[16], lx[16];
+    // this chunk's input, both row halves, taken into registers at the chunk's start so that its
+    // slot refills under the chunk's work; register 8g + 4p + i holds matrix i of column pair p
+    // of row half g
+    uint32_t ex[16];
     if (has_ein) {
       in_top_up(F, P, lane);
       const uint32_t slot = F.used % IN_SLOTS;
@@ -444,24 +440,13 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
       for (int g = 0; g < 2; ++g)
 #pragma unroll
         for (int p = 0; p < 2; ++p) ldmatrix_x4(in + sw64(16 * g + mrow, 2 * p + mcol), ex + 8 * g + 4 * p);
-      uint32_t dep = 0;
-      if (with_lo) {
-        const uint32_t slot2 = (F.used + 1) % IN_SLOTS;
-        if (!mbar_wait_or_abort(&F.full[slot2], ((F.used + 1) / IN_SLOTS) & 1, abort_flag)) return false;
-        const uint32_t inl = smem_u32(F.buf + slot2 * IN_BOX_BYTES);
-#pragma unroll
-        for (int g = 0; g < 2; ++g)
-#pragma unroll
-          for (int p = 0; p < 2; ++p) ldmatrix_x4(inl + sw64(16 * g + mrow, 2 * p + mcol), lx + 8 * g + 4 * p);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) dep ^= lx[i];
-      }
       // the loads have landed in registers (an instruction reads them all) before the warp
-      // lets lane 0 overwrite their slots
+      // lets lane 0 overwrite their slot
+      uint32_t dep = 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) dep ^= ex[i];
       asm volatile("mov.b32 %0, %0;" : "+r"(dep));
-      F.used += with_lo ? 2 : 1;
+      F.used += 1;
       __syncwarp();
       if (lane == 0) fence_proxy_async_smem();
       in_top_up(F, P, lane);
@@ -490,14 +475,19 @@ __device__ __forceinline__ bool epilogue(const NsParams& P, const EpiJob& J, uin
           } else if (EPI == EPI_POLY) {
             o0 = fmaf(cc, a0, cb * bf16_lo(ex[8 * g + k]));
             o1 = fmaf(cc, a1, cb * bf16_hi(ex[8 * g + k]));
-          } else {
-            float x0 = bf16_lo(ex[8 * g + k]), x1 = bf16_hi(ex[8 * g + k]);
-            if (with_lo) {
-              x0 += bf16_lo(lx[8 * g + k]);
-              x1 += bf16_hi(lx[8 * g + k]);
+            if (diag) {
+              // a I on the diagonal: this thread's elements sit at chunk row 16 g + 8 lo8 + lane / 4
+              // and columns 8 j + 2 (lane % 4) and the next (a diagonal chunk starts on the diagonal)
+              const int lr = 16 * g + 8 * lo8 + (lane >> 2), lc = 8 * j + 2 * (lane & 3);
+              if (lr == lc) o0 += ca;
+              if (lr == lc + 1) o1 += ca;
             }
-            o0 = J.alpha * fmaf(ca, x0, a0);
-            o1 = J.alpha * fmaf(ca, x1, a1);
+          } else if (LO == LO_READ) {
+            o0 = fmaf(ca, bf16_lo(ex[8 * g + k]), a0);   // (beta = 1 after the first step)
+            o1 = fmaf(ca, bf16_hi(ex[8 * g + k]), a1);
+          } else {
+            o0 = J.alpha * a0;
+            o1 = J.alpha * a1;
           }
           pk[k] = pack_bf16x2(o0, o1);
           // residual o - bf16(o), row-major in the (otherwise idle) transposed buffer
@@ -938,7 +928,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) ns_fused_kernel(const __grid_
         if (tk.it == 0) J.alpha = B.scale[tk.mat];
         J.st = &B.st_x[iterate_buffer(tk.it + 1)];
         // X_1's residual waits in x[2], which the second APPLY overwrites tile by tile only
-        // after each tile has read its own part (through the input ring, as input_of sets up
+        // after each chunk has read its own part (through the input ring, as input_of sets up
         // for step 1)
         if (tk.it == 0 && P.steps > 1) J.st_lo = &B.st_x[2];
         J.M = B.tall ? B.n : B.m;
