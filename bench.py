@@ -483,7 +483,7 @@ def run_native(args):
     hbm_peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     roofline = {
         "bound": "tensor",
-        "kernel": "ns_fused_kernel: all Newton-Schulz steps (A=XX^T, B=bA+cAA, X=aX+BX), %d launch(es) per step" % (
+        "kernel": "ns_fused_kernel: all Newton-Schulz steps (A=XX^T, B'=aI+bA+cAA, X=B'X), %d launch(es) per step" % (
             r["gemm_launches"] // args.steps),
         "achieved": ns_tflops, "peak": burst_peak, "unit": "TFLOP/s",
         "frac": (ns_tflops / burst_peak) if ns_tflops else None,
