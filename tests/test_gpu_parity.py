@@ -188,6 +188,26 @@ def test_newton_schulz_coefficient_schedule(nss, shape):
     assert np.array_equal(u16(wt), u16(xt))
 
 
+# steps whose b or c is zero: b A alone (c = 0), c A^2 alone (b = 0) and a I alone (both zero)
+DEGENERATE = [(3.4445, -4.7750, 2.0315), (1.5, -0.5, 0.0), (1.875, 0.0, -0.875), (1.0, 0.0, 0.0),
+              (3.4445, -4.7750, 2.0315)]
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 384), (2, 384, 256), (3, 200, 328), (2, 12, 40)])
+def test_newton_schulz_zero_coefficients(nss, shape):
+    rng = np.random.default_rng(sum(shape) + 2)
+    u = synth.to_bf16_bits(rng.standard_normal(shape))
+    ut = to_dev(u)
+    vt = torch.empty_like(ut)
+    nss.mb_newton_schulz_coeffs(ut, vt, DEGENERATE)
+    torch.cuda.synchronize()
+    assert nss.mb_sync_status() == 0
+    v = u16(vt)
+    errs = np.array([O.rel_frobenius(O.bf16_bits_to_f64(v[k]),
+                                     O.newton_schulz(O.bf16_bits_to_f64(u[k]), 5, DEGENERATE)) for k in range(shape[0])])
+    assert errs.max() <= ns_tol(*shape[1:]), errs
+
+
 def test_newton_schulz_zero_and_scaled_input(nss):
     shape = (4, 256, 256)
     u = synth.to_bf16_bits(np.random.default_rng(3).standard_normal(shape))
