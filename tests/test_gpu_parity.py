@@ -489,6 +489,29 @@ def test_deterministic(nss):
         np.testing.assert_array_equal(a, b)
 
 
+@pytest.mark.parametrize("shape", [(6, 256, 384), (5, 520, 300), (7, 6, 12)])
+def test_slot_permutation_is_bit_exact(nss, shape):
+    """Every slot of a bank is its own problem: the step on the slots permuted is the step's
+    outputs permuted, bit for bit (no slot reads another's data, scale or completion counters)."""
+    w, mant, mom, _, g = _case(44, shape, std=1.0)
+    perm = np.random.default_rng(45).permutation(shape[0])
+    while np.array_equal(perm, np.arange(shape[0])):
+        perm = np.roll(perm, 1)
+
+    def run(idx):
+        t = [to_dev(np.ascontiguousarray(x[idx])) for x in (w, mom, mant)]
+        for _ in range(2):
+            nss.muon_bank_step(t[0], to_dev(np.ascontiguousarray(g[idx])), t[1], t[2], LR, WD, MU, 5)
+        torch.cuda.synchronize()
+        assert nss.mb_sync_status() == 0
+        return [x.cpu().numpy() for x in t]
+
+    plain = run(np.arange(shape[0]))
+    permuted = run(perm)
+    for a, b in zip(plain, permuted):
+        np.testing.assert_array_equal(a[perm], b)
+
+
 def test_resume_is_bit_exact(nss):
     shape = (2, 256, 384)
     w, mant, mom, _, g = _case(41, shape)
