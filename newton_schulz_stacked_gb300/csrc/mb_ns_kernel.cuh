@@ -59,8 +59,8 @@
 //                   releases each stage in both CTAs with a multicast commit
 //   warps 2..9    : epilogue of the CTA's own 128 rows, two warps per 32-lane
 //                   TMEM quadrant (each takes half the columns); task k's
-//                   epilogue runs under task k+1's MMAs; its input (A for POLY,
-//                   X for APPLY, plus X_1's residual in the second step) arrives
+//                   epilogue runs under task k+1's MMAs; its input (A for POLY's
+//                   b A, X_1's residual in the second step's APPLY) arrives
 //                   by TMA in 32x32 boxes through a two-slot ring refilled as each
 //                   chunk is taken, and its results leave through shared memory by
 //                   TMA bulk stores; a chunk moves as 8x8 matrices in MMA-fragment
@@ -184,12 +184,12 @@ __device__ __forceinline__ Operands task_operands(const NsBank& B, const Task& k
     o.a_mn = o.b_mn = 0;
     o.K = B.m;
   } else {
-    if (!B.tall) {       // X' = a X + B X: rows of B (K-major), X as MN-major tiles
+    if (!B.tall) {       // X' = B' X: rows of B' (K-major), X as MN-major tiles
       o.a = &B.bk;
       o.b = &B.xmn2[cur];
       o.a_mn = 0;
       o.b_mn = 1;
-    } else {             // X' = a X + X B: rows of X and of B, both K-major
+    } else {             // X' = X B': rows of X and of B', both K-major
       o.a = &B.xk[cur];
       o.b = &B.bk;
       o.a_mn = 0;
@@ -374,8 +374,8 @@ __device__ __forceinline__ void in_top_up(InFeed& F, const NsParams& P, int lane
 // a diagonal 128-block the chunks below the diagonal are not stored (their
 // mirror covers them) and the chunk on the diagonal is made symmetric before
 // its store, so every element is written exactly once.
-// The input (A for POLY, X for APPLY) comes through the warp's input ring; false if a wait
-// for it ran out.
+// The input (A for POLY, X_1's residual for the second step's APPLY) comes through the warp's
+// input ring; false if a wait for it ran out.
 // fin (the last step's APPLY with LO = 0 only, a run-time choice, so that the kernel holds no
 // more inlined copies of this body than one per phase form): FIN_UPDATE also applies S5 to
 // the chunk's elements of the bank in place, each lane its own row of the chunk read back from
