@@ -177,3 +177,16 @@ def v_bits(seed: int, batch: int, rows: int, cols: int, scale: float = 1.0) -> n
     """bf16 bit patterns of an orthogonalised-update stand-in (for update-only tests)."""
     rng = _rng(seed)
     return to_bf16_bits(rng.standard_normal((batch, rows, cols), dtype=np.float32) * np.float32(scale))
+
+
+def grid_grad_bits(seed: int, batch: int, rows: int, cols: int, kmax: int = 64,
+                   quantum: float = 2.0 ** -10) -> np.ndarray:
+    """bf16 bit patterns of k * quantum with integer k drawn uniformly from [-kmax, kmax].
+
+    With kmax = 64, sums of up to three such values have |k| <= 192 < 2^8, so bf16
+    holds them exactly: any summation order over up to three ranks gives the same
+    bits (multi-rank gradient averaging tests).
+    """
+    rng = _rng(seed)
+    k = rng.integers(-kmax, kmax + 1, size=(batch, rows, cols))
+    return to_bf16_bits((k * quantum).astype(np.float32))

@@ -1,4 +1,4 @@
-"""The sharded data-parallel step's plan and data movement on two gloo CPU ranks (no GPU).
+"""The sharded data-parallel step's plan and data movement on gloo CPU ranks (no GPU).
 
 Each rank runs the local part of the step through a stand-in that applies the
 fp64 oracle's whole step to its slots (the library's CUDA path needs a GPU);
@@ -7,6 +7,12 @@ reduce-scatter of bf16 gradients and the all-gather of bf16 weights.  After two
 steps every rank's weights must equal, bit for bit, the oracle's single-rank
 step over the whole bank fed with the mean of the ranks' gradients, and each
 rank's momentum and mantissa must be the oracle's for its slots.
+
+Two ranks draw Gaussian gradients (a two-term bf16 sum is the same in either
+order).  Three ranks draw gradients on a grid of 2^-10 whose sums are exact in
+bf16, so the reduction's order cannot change the mean; there the banks split
+unevenly and the last rank owns one live slot and one padding slot of the
+first bank and only padding of the second.
 """
 import os
 import socket
@@ -53,9 +59,11 @@ def _initial(shape, seed):
     return w, mant, mom, row
 
 
-def _grad(shape, step, rank):
+def _grad(shape, step, rank, world):
     import synth
-    return synth.case(1000 + 10 * step + rank, *shape, grad_std=1e-2)[4]
+    if world == 2:
+        return synth.case(1000 + 10 * step + rank, *shape, grad_std=1e-2)[4]
+    return synth.grid_grad_bits(2000 + 10 * step + rank, *shape)
 
 
 def _oracle_local_step(banks, grads, lr, wd, mu, normuon, beta2, ns_steps, workspace):
@@ -102,7 +110,7 @@ def _worker(rank, world, port, normuon, q):
             grads = []
             for i, shape in enumerate(BANKS):
                 pad = banks[i].plan.padded - shape[0]
-                g = np.concatenate([_grad(shape, step, rank), np.zeros((pad,) + shape[1:], np.uint16)])
+                g = np.concatenate([_grad(shape, step, rank, world), np.zeros((pad,) + shape[1:], np.uint16)])
                 grads.append(torch.from_numpy(g.view(np.int16).copy()))
             sharded_step(banks, grads, LR, WD, MU, normuon=normuon, beta2=BETA2,
                          local_step=_oracle_local_step)
@@ -115,15 +123,16 @@ def _worker(rank, world, port, normuon, q):
 
 
 def _expected(world, normuon):
-    """The oracle's single-rank steps over each whole bank, fed with the ranks' mean gradient
-    (bf16 sum of the ranks' bf16 gradients, rounded once, then halved exactly for two ranks)."""
+    """The oracle's single-rank steps over each whole bank, fed with the ranks' mean gradient:
+    the bf16 sum of the ranks' bf16 gradients (one rounding for two ranks, exact on the grid
+    for three), divided by the world size in bf16."""
     import oracle as O
     out = []
     for i, shape in enumerate(BANKS):
         w, mant, mom, row = _initial(shape, 50 + i)
         w, mant, mom, row = w.copy(), mant.copy(), mom.copy(), row.copy()
         for step in (1, 2):
-            gs = [torch.from_numpy(_grad(shape, step, r).view(np.int16)).view(torch.bfloat16) for r in range(world)]
+            gs = [torch.from_numpy(_grad(shape, step, r, world).view(np.int16)).view(torch.bfloat16) for r in range(world)]
             total = gs[0].clone()
             for g in gs[1:]:
                 total = total + g
@@ -139,9 +148,9 @@ def _expected(world, normuon):
     return out
 
 
+@pytest.mark.parametrize("world", [2, 3])
 @pytest.mark.parametrize("normuon", [False, True])
-def test_two_ranks_match_the_single_rank_step(normuon):
-    world = 2
+def test_ranks_match_the_single_rank_step(world, normuon):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
